@@ -1,0 +1,38 @@
+"""Host-side checks of the seeded input generators and the work accounting."""
+
+import math
+
+import torch
+
+from tiled_attention_07_gb300 import workloads as W
+
+
+def test_named_workloads_match_their_shapes():
+    c1 = W.WORKLOADS["fp16_h1_n128_d64"]
+    x = W.make_inputs(c1)
+    assert x["q"].shape == (128, 1, 64) and x["q"].dtype == torch.float16
+    c2 = W.WORKLOADS["fp16_h16_nq1000_nk2500_d80"]
+    assert c2.shape(c2.Nq) == (1000, 16, 80) and c2.shape(c2.Nk) == (2500, 16, 80)
+    c5 = W.WORKLOADS[W.BENCH_WORKLOAD]
+    assert c5.backward and c5.causal and c5.shape(c5.Nq) == (4, 32, 8192, 80)
+    assert abs(c5.sm_scale - 1 / math.sqrt(80)) < 1e-15
+
+
+def test_generator_is_seeded_and_distribution_is_right():
+    w = W.custom("bf16", "bhsd", 2, 3, 300, 200, 64, False, std=0.5, seed=7, backward=True)
+    a = W.make_inputs(w)
+    b = W.make_inputs(w)
+    for key in ("q", "k", "v", "do"):
+        assert torch.equal(a[key], b[key])
+    q = a["q"].float()
+    assert abs(q.std().item() - 0.5) < 0.01 and abs(q.mean().item()) < 0.01
+    assert abs(a["do"].float().std().item() - 1.0) < 0.02
+    assert not torch.equal(a["q"], a["k"])
+
+
+def test_flop_accounting():
+    w = W.custom("bf16", "bhsd", 4, 32, 8192, 8192, 80, True)
+    assert w.fwd_flops() == 4 * 4 * 32 * 8192 * 8192 * 80 / 2
+    assert w.bwd_flops() == 2.5 * w.fwd_flops()
+    w2 = W.custom("fp16", "shd", 1, 16, 1000, 2500, 80, False)
+    assert w2.fwd_flops() == 4 * 16 * 1000 * 2500 * 80
