@@ -1,0 +1,439 @@
+#!/usr/bin/env python
+"""Throughput of the FlashAttention-2 hot path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic input:
+the forward (fa_fwd: O and LSE) and the recompute backward (fa_bwd's three
+launches: D/LSE preprocess, dK/dV pass, dQ pass), on the workload
+bf16, causal, B=4, H=32, N=8192, d=80 (the only workload that takes the
+backward too).  Throughput is credited TFLOP/s: forward 4*B*H*N^2*d/2 and
+backward 10*B*H*N^2*d/2 per step (causal halves both), i.e. five GEMMs for
+the backward even though the two-pass backward executes seven.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line (rank 0).  With N > 1 (under torchrun) every rank runs
+its own copy of the workload (independent heads need no exchange: weak
+scaling, no collective on the data path) and the timing is the max over
+ranks.  ``--impl reference`` times the float64 CPU oracle instead, on a
+bounded sample of the same workload per step.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd/bwd TFLOP/s on 1 GB300 and fraction of dense BF16 tensor peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=None, help="workload name (default: the fwd+bwd bench workload)")
+    ap.add_argument("--batch", type=int, default=None, help="override the workload's batch size (small profiling cases)")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (weak scaling: one independent replica per rank)
+# ---------------------------------------------------------------------------
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    rank = dist.get_rank() if world > 1 else 0
+    return rank, world
+
+
+def reduce_max(value: float, device=None) -> float:
+    """Max of a float over all ranks (identity with one process)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self):
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        dev = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        if dev.isdigit():
+            cmd[1:1] = ["-i", dev]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) == 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if rows:
+            first = rows[0][0]
+            rows = [r for r in rows if r[0] == first]
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "", 1).isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "", 1).isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def committed_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if any
+    (a line ``traffic_bytes_per_launch <kernel> <bytes> <source-hash>``)."""
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    try:
+        with open(path) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) >= 3 and parts[0] == "traffic_bytes_per_launch" and parts[1] == kernel:
+                    return float(parts[2])
+    except OSError:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------------------
+# the CUDA path
+# ---------------------------------------------------------------------------
+
+def per_kernel_flops(w):
+    """Algorithmic FLOPs per launch of each kernel (GEMMs the kernel performs)."""
+    pd = w.pairs() * w.d
+    return {"fwd": 4.0 * pd, "bwd_pre": 0.0, "bwd_dkdv": 8.0 * pd, "bwd_dq": 6.0 * pd}
+
+
+def pick_workload(args):
+    import dataclasses
+
+    from tiled_attention_07_gb300 import workloads as W
+
+    w = W.WORKLOADS[args.workload or W.BENCH_WORKLOAD]
+    if args.batch is not None and args.batch != w.B:
+        w = dataclasses.replace(w, B=args.batch, name=f"{w.name}_b{args.batch}")
+    return w
+
+
+def run_ours(args):
+    import torch
+
+    from tiled_attention_07_gb300 import fa
+    from tiled_attention_07_gb300 import workloads as W
+
+    rank, world = dist_init("nccl")
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = pick_workload(args)
+    host = W.make_inputs(w, device="cpu", with_grad_output=True)
+    x = {k: t.to(dev) for k, t in host.items()}
+    q, k, v, do = x["q"], x["k"], x["v"], x["do"]
+    o = torch.empty_like(q)
+    lse = torch.empty(fa.lse_shape(q), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    B, H, Nq, d = fa._dims(q)
+    Nk = fa._dims(k)[2]
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, Nq, Nk, d), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    names = ("fwd", "bwd_pre", "bwd_dkdv", "bwd_dq")
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        fa.fa_fwd(q, k, v, o, lse, w.sm_scale, w.causal, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        for i, phase in enumerate((fa.FA_BWD_PREPROCESS, fa.FA_BWD_DKDV, fa.FA_BWD_DQ)):
+            fa.fa_bwd_phase(phase, q, k, v, o, do, lse, dq, dk, dv, w.sm_scale, w.causal, ws, stream)
+            if ev is not None:
+                ev[2 + i].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    rc, detail = fa.fa_last_device_error(stream)
+    if rc != fa.FA_OK:
+        raise RuntimeError(f"device error after warm-up: {detail:#x}")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler() if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize(dev)
+    t0.record(stream)
+    for i in range(K):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clk = clocks.stop() if clocks else None
+    rc, detail = fa.fa_last_device_error(stream)
+    if rc != fa.FA_OK:
+        raise RuntimeError(f"device error in the timed region: {detail:#x}")
+
+    ms = reduce_max(t0.elapsed_time(t1), dev)
+    ms_step = ms / K
+    step_flops = w.fwd_flops() + w.bwd_flops()
+    value = world * K * step_flops / (ms / 1e3) / 1e12
+    kern_ms = {n: sum(e[j].elapsed_time(e[j + 1]) for e in evs) / K for j, n in enumerate(names)}
+    peaks, peak_src = load_peaks()
+    peak = peaks["bf16_tflops_sustained"]
+    kflops = per_kernel_flops(w)
+    kernels = {}
+    for n in names:
+        entry = {"ms": round(kern_ms[n], 4), "share": round(kern_ms[n] / sum(kern_ms.values()), 4)}
+        if kflops[n] > 0:
+            entry["tflops"] = round(kflops[n] / (kern_ms[n] / 1e3) / 1e12, 2)
+            entry["frac"] = round(entry["tflops"] / peak, 4)
+        kernels[n] = entry
+    dom = max((n for n in names if kflops[n] > 0), key=lambda n: kern_ms[n])
+    achieved = kflops[dom] / (kern_ms[dom] / 1e3) / 1e12
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": committed_traffic(dom),
+                "peak_source": f"{peak_src} bf16 sustained (kernel timed inside back-to-back steps)"}
+    fwd_tf = w.fwd_flops() / (kern_ms["fwd"] / 1e3) / 1e12
+    bwd_ms = kern_ms["bwd_pre"] + kern_ms["bwd_dkdv"] + kern_ms["bwd_dq"]
+    bwd_tf = w.bwd_flops() / (bwd_ms / 1e3) / 1e12
+    passes = {"fwd": {"tflops": round(fwd_tf, 2), "frac_of_peak": round(fwd_tf / peak, 4)},
+              "bwd": {"tflops_credited": round(bwd_tf, 2), "frac_of_peak": round(bwd_tf / peak, 4)}}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, host, dev, stream, world)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, host)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "fp16",
+        "data": "synthetic (seeded N(0,1) q, k, v, dO)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
+                   "causal": w.causal, "sm_scale": w.sm_scale, "layout": w.layout,
+                   "step": "fa_fwd + fa_bwd (preprocess, dK/dV pass, dQ pass)",
+                   "flops_per_step": step_flops, "l2": "inputs larger than L2 (each of q, k, v, dO is "
+                   f"{q.numel() * 2 / 1e6:.0f} MB > 129 MB)", "parallelism": f"replica x{world}"},
+        "roofline": roofline, "kernels": kernels, "passes": passes,
+        "clocks": clk, "gpu_launches": 4 * K,
+        "e2e": e2e, "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, w, host, dev, stream, world):
+    """Same metric through the public API with host buffers: every step copies
+    q, k, v, dO from pinned host memory, runs forward and backward, and copies
+    O, LSE, dQ, dK, dV back to pinned host memory."""
+    import torch
+
+    from tiled_attention_07_gb300 import fa
+
+    pin = {k: t.pin_memory() for k, t in host.items()}
+    dx = {k: torch.empty_like(t, device=dev) for k, t in host.items()}
+    q, k, v, do = dx["q"], dx["k"], dx["v"], dx["do"]
+    o = torch.empty_like(q)
+    lse = torch.empty(fa.lse_shape(q), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    B, H, Nq, d = fa._dims(q)
+    Nk = fa._dims(k)[2]
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, Nq, Nk, d), dtype=torch.uint8, device=dev)
+    outs = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+    hout = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in outs.items()}
+
+    def step():
+        for n in ("q", "k", "v", "do"):
+            dx[n].copy_(pin[n], non_blocking=True)
+        fa.fa_fwd(q, k, v, o, lse, w.sm_scale, w.causal, stream)
+        fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, w.sm_scale, w.causal, ws, stream)
+        for n, t in outs.items():
+            hout[n].copy_(t, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize(dev)
+    K = max(1, args.e2e_steps)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    t0.record(stream)
+    for _ in range(K):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    ms = reduce_max(t0.elapsed_time(t1), dev)
+    value = world * K * (w.fwd_flops() + w.bwd_flops()) / (ms / 1e3) / 1e12
+    bi = sum(t.numel() * t.element_size() for t in pin.values())
+    bo = sum(t.numel() * t.element_size() for t in hout.values())
+    return {"value": round(value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            "steps": K, "ms_per_step": round(ms / K, 3)}
+
+
+# ---------------------------------------------------------------------------
+# the float64 CPU oracle (reported baseline)
+# ---------------------------------------------------------------------------
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _head64(t, layout, b, h, n=None):
+    from tiled_attention_07_gb300 import workloads as W
+
+    m = W.head_view(t, layout, b, h)
+    if n is not None:
+        m = m[:n]
+    return m.double().numpy()
+
+
+def cpu_baseline(w, host):
+    """The oracle, as it stands, on one full (b, h) head of the workload."""
+    import oracle.attention as ref
+
+    q, k, v, do = (_head64(host[n], w.layout, 0, 0) for n in ("q", "k", "v", "do"))
+    t = time.perf_counter()
+    ref.forward(q, k, v, w.sm_scale, w.causal)
+    ref.backward(q, k, v, do, w.sm_scale, w.causal)
+    sec = time.perf_counter() - t
+    pairs = w.Nq * w.Nk * (0.5 if w.causal else 1.0)
+    flops = 14.0 * pairs * w.d   # credited fwd (4) + bwd (10) per pair
+    return {"value": round(flops / sec / 1e12, 6), "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
+            "sample": f"head (0,0) of {w.name}: full {w.Nq}x{w.Nk} fwd+bwd in float64 numpy, "
+                      f"{sec:.2f} s"}
+
+
+def run_reference(args):
+    """The oracle timed on the host cores (rank 0 only); each step is the
+    forward + backward of the top-left 2048 x 2048 block of one head (the
+    exact causal sub-problem of its first 2048 queries), heads in turn."""
+    rank, world = dist_init("gloo")
+    if rank != 0:
+        return
+    import oracle.attention as ref
+    from tiled_attention_07_gb300 import workloads as W
+
+    w = pick_workload(args)
+    host = W.make_inputs(w, device="cpu", with_grad_output=True)
+    n = min(2048, w.Nq, w.Nk)
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+
+    def step(i):
+        b, h = heads[i % len(heads)]
+        q, k, v, do = (_head64(host[m], w.layout, b, h, n) for m in ("q", "k", "v", "do"))
+        ref.forward(q, k, v, w.sm_scale, w.causal)
+        ref.backward(q, k, v, do, w.sm_scale, w.causal)
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    t = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    sec = time.perf_counter() - t
+    pairs = n * n * (0.5 if w.causal else 1.0)
+    flops = 14.0 * pairs * w.d
+    value = args.steps * flops / sec / 1e12
+    sample = f"per step: top-left {n}x{n} causal block of one head of {w.name}, fwd+bwd in float64 numpy"
+    line = {"metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": round(sec / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1) q, k, v, dO)", "impl": "reference",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
+                       "causal": w.causal},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": _cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

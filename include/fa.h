@@ -1,0 +1,177 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) FlashAttention-2 library (libfa.so).
+ *
+ * Exact attention, forward and recompute-based backward:
+ *
+ *   S = sm_scale * Q K^T  [+ causal mask],  P = softmax_row(S),  O = P V,
+ *   LSE_i = log sum_j exp(S_ij),
+ *   dV = P^T dO,  dP = dO V^T,  D = rowsum(O o dO),  dS = P o (dP - D),
+ *   dQ = sm_scale dS K,  dK = sm_scale dS^T Q.
+ *
+ * Sources: "[CS336] Assignment 2: Systems", section "FlashAttention V2"
+ * (High level: the forward and backward equations, the logsumexp L and the
+ * precomputed D; Forward Pass: the online running max / running sum over key
+ * tiles; Backward Pass: the two accumulation directions).  "Understanding
+ * Triton Tutorials Part 2", section "Fused Attention 2" (exp2 with sm_scale
+ * folded by log2(e), causal block skipping, the [Z, H, N_CTX, HEAD_DIM]
+ * layout).  "BUG in flash attention kernel" (triton issue 2626): the
+ * [seq, heads, d] layout with Nq != Nk, and per-tensor strides.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *   never allocates, frees or keeps device memory of its own apart from one
+ *   4-byte error word per device.  Outputs are fully overwritten (no
+ *   accumulate-into semantics), so they need no zeroing.
+ * - Element type: FA_FP16 or FA_BF16 for Q, K, V, O, dO, dQ, dK, dV; the
+ *   log-sum-exp is always float32.  Arithmetic is fp32 accumulation on the
+ *   tensor cores, P and dS are rounded to the input type before their GEMMs.
+ * - Layout: each Q/K/V/O-like tensor is addressed as x[b, h, s, 0..d-1] at
+ *   element offset b*stride_b + h*stride_h + s*stride_s, with the head
+ *   dimension contiguous (stride 1).  fa_fwd / fa_bwd assume contiguous
+ *   [B, H, seq, d]; the *_strided variants take explicit strides (e.g.
+ *   [seq, heads, d] is B = 1, stride_h = d, stride_s = H*d).
+ * - lse (and the backward's lse input) is float32 [B, H, Nq] contiguous, the
+ *   natural log of sum_j exp(sm_scale * q_i . k_j) over the visible keys.
+ * - Causal masking is top-left aligned: key j is visible to query i iff
+ *   j <= i, also when Nq != Nk.
+ * - Requirements (checked before any launch): B, H, Nq >= 0; Nk >= 1;
+ *   d in {64, 80, 128}; pointers non-null and 16-byte aligned; strides
+ *   (in bytes) multiples of 16; sm_scale finite and > 0.  B*H == 0 or Nq == 0 is a
+ *   no-op returning FA_OK.  Other d give FA_ERR_UNSUPPORTED.
+ * - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *   default stream) and never synchronise.  The return value reports
+ *   argument errors (nothing launched) and launch errors (FA_ERR_CUDA).
+ * - Every device-side wait is bounded.  A wait that runs out records a code in
+ *   the per-device error word and the kernel finishes without hanging;
+ *   fa_last_device_error() reports it.
+ * - Thread safety: entry points may be called from several host threads.
+ */
+#ifndef TILED_ATTENTION_07_GB300_FA_H
+#define TILED_ATTENTION_07_GB300_FA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,   /* bad pointer, size, stride, alignment or scale */
+    FA_ERR_UNSUPPORTED = 2,   /* valid but not implemented (head dim, dtype)   */
+    FA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed             */
+    FA_ERR_TIMEOUT = 4,       /* a bounded device-side wait ran out            */
+    FA_ERR_WORKSPACE = 5      /* backward workspace missing or too small       */
+} fa_status;
+
+typedef enum { FA_FP16 = 0, FA_BF16 = 1 } fa_dtype;
+
+/* Element strides of one [B, H, seq, d] tensor; the d stride is always 1. */
+typedef struct {
+    int64_t b, h, s;
+} fa_strides;
+
+/* Strides of every tensor an entry point touches; entries it does not use are
+ * ignored. */
+typedef struct {
+    fa_strides q, k, v, o, dout, dq, dk, dv;
+} fa_layout;
+
+/*
+ * fa_fwd -- FlashAttention-2 forward ("[CS336]", "FlashAttention V2 /
+ * Forward Pass"; "Fused Attention 2", _attn_fwd).
+ *   q   [B, H, Nq, d]   in          k, v [B, H, Nk, d]  in
+ *   o   [B, H, Nq, d]   out         lse  [B, H, Nq] float32 out
+ *   sm_scale: multiplies q.k before the softmax; causal: 0 or 1.
+ * Returns FA_OK or an error code (see the conventions above).
+ */
+FA_API fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int H, int Nq, int Nk, int d, float sm_scale, int causal,
+                 fa_dtype dtype, void* stream);
+
+/* fa_fwd with explicit strides for q, k, v and o (layout->q, ->k, ->v, ->o);
+ * e.g. the [seq, heads, d] layout of "BUG in flash attention kernel"
+ * (B = 1, stride_h = d, stride_s = heads*d).  lse stays [B, H, Nq]. */
+FA_API fa_status fa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int B, int H, int Nq, int Nk, int d, float sm_scale, int causal,
+                         fa_dtype dtype, const fa_layout* layout, void* stream);
+
+/*
+ * fa_bwd_workspace_bytes -- size of the scratch buffer fa_bwd needs: the
+ * per-row D = rowsum(O o dO) and the log2-domain LSE, float32, padded to
+ * whole 128-row query tiles: 2 * 4 * B*H*ceil(Nq/128)*128 bytes.
+ */
+FA_API size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int Nk, int d);
+
+/*
+ * fa_bwd -- recompute-based backward ("[CS336]", "FlashAttention V2 /
+ * Backward Pass": P_ij = exp(S_ij - L_i), dS = P o (dP - D), the two passes
+ * over K tiles (dQ) and Q tiles (dK, dV)).
+ *   q, k, v, o, dout: as produced/consumed by fa_fwd (o is fa_fwd's output)
+ *   lse: float32 [B, H, Nq] from fa_fwd
+ *   dq [B, H, Nq, d], dk, dv [B, H, Nk, d]: out, input dtype
+ *   workspace: device buffer of at least fa_bwd_workspace_bytes() bytes,
+ *   16-byte aligned, owned by the caller; its contents on entry are ignored.
+ * Returns FA_ERR_WORKSPACE if the workspace is NULL or too small.
+ */
+FA_API fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                 const float* lse, void* dq, void* dk, void* dv,
+                 int B, int H, int Nq, int Nk, int d, float sm_scale, int causal,
+                 fa_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/* fa_bwd with explicit strides (layout->q, k, v, o, dout, dq, dk, dv). */
+FA_API fa_status fa_bwd_strided(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                         const float* lse, void* dq, void* dk, void* dv,
+                         int B, int H, int Nq, int Nk, int d, float sm_scale, int causal,
+                         fa_dtype dtype, const fa_layout* layout,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * fa_bwd_phase -- one of the three launches fa_bwd makes, for callers that
+ * schedule or time them separately ("[CS336]", "FlashAttention V2 / Backward
+ * Pass": D precomputed in global memory before the backward, then the dQ pass
+ * over key tiles and the dK/dV pass over query tiles):
+ *   phase FA_BWD_PREPROCESS (1): D = rowsum(O o dO) and LSE*log2(e) into the
+ *                                workspace (reads o, dout, lse)
+ *   phase FA_BWD_DKDV (2):       dk, dv (reads q, k, v, dout, workspace)
+ *   phase FA_BWD_DQ (3):         dq (reads q, k, v, dout, workspace)
+ * Calling phases 1, 2, 3 in order on one stream, with the same workspace, is
+ * exactly fa_bwd.  layout == NULL means contiguous [B, H, seq, d] tensors.
+ * Other arguments, requirements and errors as fa_bwd / fa_bwd_strided; an
+ * unknown phase gives FA_ERR_INVALID_ARG.
+ */
+enum { FA_BWD_PREPROCESS = 1, FA_BWD_DKDV = 2, FA_BWD_DQ = 3 };
+FA_API fa_status fa_bwd_phase(int phase, const void* q, const void* k, const void* v, const void* o,
+                       const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                       int B, int H, int Nq, int Nk, int d, float sm_scale, int causal,
+                       fa_dtype dtype, const fa_layout* layout,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+FA_API const char* fa_status_string(fa_status status);
+
+/*
+ * fa_last_device_error -- synchronises `stream`, then reads and clears the
+ * current device's error word.  Returns FA_ERR_TIMEOUT if a kernel gave up a
+ * bounded wait since the last call, FA_ERR_CUDA if the synchronisation
+ * failed, else FA_OK.  *detail (if non-NULL) receives the raw device code
+ * (which wait gave up), 0 if none.
+ */
+FA_API fa_status fa_last_device_error(void* stream, int* detail);
+
+/* Library version string, e.g. "0.1.0". */
+FA_API const char* fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TILED_ATTENTION_07_GB300_FA_H */

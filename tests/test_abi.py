@@ -1,0 +1,128 @@
+"""The C ABI library loads, exports every symbol include/fa.h declares, and
+rejects bad arguments before touching the GPU (these calls make no CUDA call,
+so they run on a machine without a GPU)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from tiled_attention_07_gb300 import fa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+def header_symbols():
+    text = open(HEADER).read()
+    return re.findall(r"FA_API\s+[\w\s\*]+?\b(fa_\w+)\s*\(", text)
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(fa.LIB_PATH):
+        from tiled_attention_07_gb300 import build
+        build.build()
+    return fa.lib()
+
+
+def test_header_declares_the_binding_symbols():
+    syms = header_symbols()
+    assert sorted(syms) == sorted(fa.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for s in header_symbols():
+        assert hasattr(L, s), f"libfa.so does not export {s}"
+
+
+def test_status_strings_and_version(L):
+    assert fa.fa_version() == "0.1.0"
+    for code in range(6):
+        assert fa.fa_status_string(code).startswith("FA_")
+    assert "unknown" in fa.fa_status_string(99)
+
+
+def test_workspace_bytes(L):
+    assert fa.fa_bwd_workspace_bytes(4, 32, 8192, 8192, 80) == 2 * 4 * 4 * 32 * 8192
+    assert fa.fa_bwd_workspace_bytes(1, 16, 1000, 2500, 80) == 2 * 4 * 16 * 1024
+    assert fa.fa_bwd_workspace_bytes(0, 16, 1000, 2500, 80) == 0
+    assert fa.fa_bwd_workspace_bytes(2, 3, 0, 5, 64) == 0
+
+
+FAKE = 1 << 20  # a 16-byte aligned non-null address; never dereferenced here
+
+
+def fwd(L, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=1, Nq=128, Nk=128, d=64, scale=0.125, causal=0,
+        dtype=fa.FA_BF16):
+    return L.fa_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, dtype, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=32), fa.FA_ERR_UNSUPPORTED),
+    (dict(dtype=7), fa.FA_ERR_UNSUPPORTED),
+    (dict(Nk=0), fa.FA_ERR_INVALID_ARG),
+    (dict(Nq=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(B=-2), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=0.0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=-1.0), fa.FA_ERR_INVALID_ARG),
+    (dict(causal=2), fa.FA_ERR_INVALID_ARG),
+    (dict(q=None), fa.FA_ERR_INVALID_ARG),
+    (dict(o=None), fa.FA_ERR_INVALID_ARG),
+    (dict(lse=None), fa.FA_ERR_INVALID_ARG),
+    (dict(k=FAKE + 8), fa.FA_ERR_INVALID_ARG),
+    (dict(lse=FAKE + 4), fa.FA_ERR_INVALID_ARG),
+])
+def test_fwd_rejects_bad_arguments(L, kw, code):
+    assert fwd(L, **kw) == code
+
+
+def test_fwd_empty_problems_are_noops(L):
+    assert fwd(L, B=0) == fa.FA_OK
+    assert fwd(L, H=0) == fa.FA_OK
+    assert fwd(L, Nq=0) == fa.FA_OK
+    assert fwd(L, Nq=0, q=None, o=None, lse=None) == fa.FA_OK
+
+
+def test_strided_rejects_bad_strides(L):
+    lay = fa.Layout()
+    for n in ("q", "k", "v", "o"):
+        setattr(lay, n, fa.Strides(128 * 64, 128 * 64, 64))
+    args = [FAKE] * 5 + [1, 1, 128, 128, 64, 0.125, 0, fa.FA_BF16]
+    lay.k = fa.Strides(128 * 64, 128 * 64, 60)   # 120-byte rows: not a multiple of 16
+    assert L.fa_fwd_strided(*args, ctypes.byref(lay), None) == fa.FA_ERR_INVALID_ARG
+    lay.k = fa.Strides(128 * 64, 0, 64)
+    assert L.fa_fwd_strided(*args, ctypes.byref(lay), None) == fa.FA_ERR_INVALID_ARG
+    assert L.fa_fwd_strided(*args, None, None) == fa.FA_ERR_INVALID_ARG
+
+
+def bwd(L, ws=FAKE, ws_bytes=1 << 30, d=64, Nk=128, **kw):
+    ptrs = [FAKE] * 9
+    return L.fa_bwd(*ptrs, 1, 1, 128, Nk, d, 0.125, 0, fa.FA_BF16, ws, ws_bytes, None)
+
+
+def test_bwd_phase_rejects_unknown_phase(L):
+    ptrs = [FAKE] * 9
+    for phase in (0, 4, -1):
+        assert L.fa_bwd_phase(phase, *ptrs, 1, 1, 128, 128, 64, 0.125, 0, fa.FA_BF16, None, FAKE, 1 << 20,
+                              None) == fa.FA_ERR_INVALID_ARG
+
+
+def test_bwd_checks_workspace_and_args(L):
+    need = fa.fa_bwd_workspace_bytes(1, 1, 128, 128, 64)
+    assert bwd(L, ws=None) == fa.FA_ERR_WORKSPACE
+    assert bwd(L, ws_bytes=need - 16) == fa.FA_ERR_WORKSPACE
+    assert bwd(L, ws=FAKE + 4) == fa.FA_ERR_WORKSPACE
+    assert bwd(L, d=100) == fa.FA_ERR_UNSUPPORTED
+    assert bwd(L, Nk=0) == fa.FA_ERR_INVALID_ARG
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.attention_forward(q, q, q, 0.125, False)

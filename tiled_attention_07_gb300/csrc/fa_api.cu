@@ -1,0 +1,297 @@
+// fa_api.cu -- the C ABI of libfa.so: argument validation, TMA map encoding,
+// the per-device error word, and dispatch to the forward / backward launchers.
+// Declarations and the contract of every entry point are in include/fa.h.
+#include "../../include/fa.h"
+#include "fa_internal.h"
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+namespace fa {
+
+// Device error word: written by kernels whose bounded waits gave up.
+__device__ int g_err_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+std::mutex g_mu;
+int* g_err_ptr[kMaxDevices];   // device address of g_err_word per device
+bool g_err_init[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+bool g_encode_tried = false;
+
+EncodeTiledFn get_encode() {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_encode_tried) {
+    g_encode_tried = true;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  return g_encode;
+}
+
+// Address of this device's error word (looked up once per device).
+int* err_word(cudaError_t* e) {
+  int dev = 0;
+  *e = cudaGetDevice(&dev);
+  if (*e != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= kMaxDevices) {
+    *e = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_err_init[dev]) {
+    void* ptr = nullptr;
+    *e = cudaGetSymbolAddress(&ptr, g_err_word);
+    if (*e != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<int*>(ptr);
+    g_err_init[dev] = true;
+  }
+  return g_err_ptr[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// A [B, H, rows, d] tensor view is valid for TMA and 16-byte vector access.
+bool valid_tensor(const Tensor4& t) {
+  if (t.ptr == nullptr || !aligned16(t.ptr)) return false;
+  const int64_t st[3] = {t.sb, t.sh, t.ss};
+  for (int64_t s : st) {
+    if (s <= 0) return false;
+    if ((s * 2) % 16 != 0) return false;
+    if (s * 2 >= (int64_t(1) << 40)) return false;
+  }
+  return true;
+}
+
+fa_status check_common(int B, int H, int Nq, int Nk, int d, float sm_scale, int causal, fa_dtype dtype) {
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 1) return FA_ERR_INVALID_ARG;
+  if (!(std::isfinite(sm_scale)) || !(sm_scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 80 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(B) * H > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+Tensor4 contiguous(const void* p, int H, int n, int d) {
+  Tensor4 t;
+  t.ptr = p;
+  t.ss = d;
+  t.sh = static_cast<int64_t>(n) * d;
+  t.sb = static_cast<int64_t>(H) * n * d;
+  return t;
+}
+
+Tensor4 strided(const void* p, const fa_strides& s) {
+  Tensor4 t;
+  t.ptr = p;
+  t.sb = s.b;
+  t.sh = s.h;
+  t.ss = s.s;
+  return t;
+}
+
+fa_status fwd_impl(const Tensor4& q, const Tensor4& k, const Tensor4& v, const Tensor4& o, float* lse, int B, int H,
+                   int Nq, int Nk, int d, float sm_scale, int causal, fa_dtype dtype, void* stream) {
+  fa_status st = check_common(B, H, Nq, Nk, d, sm_scale, causal, dtype);
+  if (st != FA_OK) return st;
+  if (B == 0 || H == 0 || Nq == 0) return FA_OK;
+  if (!valid_tensor(q) || !valid_tensor(k) || !valid_tensor(v) || !valid_tensor(o)) return FA_ERR_INVALID_ARG;
+  if (lse == nullptr || !aligned16(lse)) return FA_ERR_INVALID_ARG;
+  if (get_encode() == nullptr) return FA_ERR_CUDA;
+  cudaError_t e;
+  int* err = err_word(&e);
+  if (err == nullptr) return FA_ERR_CUDA;
+  FwdArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.H = H;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.d = d;
+  a.sm_scale = sm_scale;
+  a.causal = causal;
+  a.bf16 = dtype == FA_BF16;
+  a.err = err;
+  e = launch_fwd(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t ws_bytes(int B, int H, int Nq) {
+  if (B <= 0 || H <= 0 || Nq <= 0) return 0;
+  return 2 * sizeof(float) * static_cast<size_t>(B) * H * nq_pad(Nq);
+}
+
+fa_status bwd_impl(const Tensor4& q, const Tensor4& k, const Tensor4& v, const Tensor4& o, const Tensor4& dout,
+                   const float* lse, const Tensor4& dq, const Tensor4& dk, const Tensor4& dv, int B, int H, int Nq,
+                   int Nk, int d, float sm_scale, int causal, fa_dtype dtype, void* workspace,
+                   size_t workspace_bytes, int phase, void* stream) {
+  if (phase < 0 || phase > 3) return FA_ERR_INVALID_ARG;
+  fa_status st = check_common(B, H, Nq, Nk, d, sm_scale, causal, dtype);
+  if (st != FA_OK) return st;
+  if (B == 0 || H == 0) return FA_OK;
+  // With no queries only dK = dV = 0 is written; the query-side tensors, lse
+  // and the workspace are not touched.
+  if (!valid_tensor(k) || !valid_tensor(v) || !valid_tensor(dk) || !valid_tensor(dv)) return FA_ERR_INVALID_ARG;
+  if (Nq > 0) {
+    if (!valid_tensor(q) || !valid_tensor(o) || !valid_tensor(dout) || !valid_tensor(dq))
+      return FA_ERR_INVALID_ARG;
+    if (lse == nullptr || !aligned16(lse)) return FA_ERR_INVALID_ARG;
+    if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < ws_bytes(B, H, Nq))
+      return FA_ERR_WORKSPACE;
+  }
+  if (get_encode() == nullptr) return FA_ERR_CUDA;
+  cudaError_t e;
+  int* err = err_word(&e);
+  if (err == nullptr) return FA_ERR_CUDA;
+  BwdArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.dout = dout;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.lse = lse;
+  a.ws = static_cast<float*>(workspace);
+  a.B = B;
+  a.H = H;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.d = d;
+  a.sm_scale = sm_scale;
+  a.causal = causal;
+  a.bf16 = dtype == FA_BF16;
+  a.err = err;
+  e = launch_bwd(a, phase, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+bool make_tile_map(CUtensorMap* map, const Tensor4& t, int d, int rows, int H, int B, bool bf16) {
+  EncodeTiledFn enc = get_encode();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(t.ss * 2), static_cast<cuuint64_t>(t.sh * 2),
+                                 static_cast<cuuint64_t>(t.sb * 2)};
+  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(kTileRows), 1, 1};
+  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+                   const_cast<void*>(t.ptr), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace fa
+
+using fa::Tensor4;
+
+extern "C" {
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
+                 int d, float sm_scale, int causal, fa_dtype dtype, void* stream) {
+  return fa::fwd_impl(fa::contiguous(q, H, Nq, d), fa::contiguous(k, H, Nk, d), fa::contiguous(v, H, Nk, d),
+                      fa::contiguous(o, H, Nq, d), lse, B, H, Nq, Nk, d, sm_scale, causal, dtype, stream);
+}
+
+fa_status fa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                         int Nk, int d, float sm_scale, int causal, fa_dtype dtype, const fa_layout* layout,
+                         void* stream) {
+  if (layout == nullptr) return FA_ERR_INVALID_ARG;
+  return fa::fwd_impl(fa::strided(q, layout->q), fa::strided(k, layout->k), fa::strided(v, layout->v),
+                      fa::strided(o, layout->o), lse, B, H, Nq, Nk, d, sm_scale, causal, dtype, stream);
+}
+
+size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
+  (void)Nk;
+  (void)d;
+  return fa::ws_bytes(B, H, Nq);
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                 void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float sm_scale, int causal,
+                 fa_dtype dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  return fa::bwd_impl(fa::contiguous(q, H, Nq, d), fa::contiguous(k, H, Nk, d), fa::contiguous(v, H, Nk, d),
+                      fa::contiguous(o, H, Nq, d), fa::contiguous(dout, H, Nq, d), lse,
+                      fa::contiguous(dq, H, Nq, d), fa::contiguous(dk, H, Nk, d), fa::contiguous(dv, H, Nk, d), B,
+                      H, Nq, Nk, d, sm_scale, causal, dtype, workspace, workspace_bytes, 0, stream);
+}
+
+fa_status fa_bwd_strided(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                         const float* lse, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
+                         float sm_scale, int causal, fa_dtype dtype, const fa_layout* layout, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  if (layout == nullptr) return FA_ERR_INVALID_ARG;
+  return fa::bwd_impl(fa::strided(q, layout->q), fa::strided(k, layout->k), fa::strided(v, layout->v),
+                      fa::strided(o, layout->o), fa::strided(dout, layout->dout), lse,
+                      fa::strided(dq, layout->dq), fa::strided(dk, layout->dk), fa::strided(dv, layout->dv), B, H,
+                      Nq, Nk, d, sm_scale, causal, dtype, workspace, workspace_bytes, 0, stream);
+}
+
+fa_status fa_bwd_phase(int phase, const void* q, const void* k, const void* v, const void* o, const void* dout,
+                       const float* lse, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d,
+                       float sm_scale, int causal, fa_dtype dtype, const fa_layout* layout, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  if (phase < 1 || phase > 3) return FA_ERR_INVALID_ARG;
+  if (layout == nullptr)
+    return fa::bwd_impl(fa::contiguous(q, H, Nq, d), fa::contiguous(k, H, Nk, d), fa::contiguous(v, H, Nk, d),
+                        fa::contiguous(o, H, Nq, d), fa::contiguous(dout, H, Nq, d), lse,
+                        fa::contiguous(dq, H, Nq, d), fa::contiguous(dk, H, Nk, d), fa::contiguous(dv, H, Nk, d),
+                        B, H, Nq, Nk, d, sm_scale, causal, dtype, workspace, workspace_bytes, phase, stream);
+  return fa::bwd_impl(fa::strided(q, layout->q), fa::strided(k, layout->k), fa::strided(v, layout->v),
+                      fa::strided(o, layout->o), fa::strided(dout, layout->dout), lse,
+                      fa::strided(dq, layout->dq), fa::strided(dk, layout->dk), fa::strided(dv, layout->dv), B, H,
+                      Nq, Nk, d, sm_scale, causal, dtype, workspace, workspace_bytes, phase, stream);
+}
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: bad pointer, size, stride, alignment or scale";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dim or dtype not supported";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call failed";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a bounded device-side wait ran out";
+    case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: backward workspace missing or too small";
+  }
+  return "unknown fa_status";
+}
+
+fa_status fa_last_device_error(void* stream, int* detail) {
+  if (detail) *detail = 0;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, fa::g_err_word, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(fa::g_err_word, &zero, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+  }
+  if (detail) *detail = v;
+  return v != 0 ? FA_ERR_TIMEOUT : FA_OK;
+}
+
+const char* fa_version(void) { return "0.1.0"; }
+
+}  // extern "C"

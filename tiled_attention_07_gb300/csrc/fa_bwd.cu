@@ -1,0 +1,777 @@
+// fa_bwd.cu -- recompute-based FlashAttention-2 backward for sm_103a.
+//
+// "[CS336] Assignment 2: Systems", "FlashAttention V2 / High level" and
+// "Backward Pass": with the saved LSE L and D = rowsum(O o dO) precomputed in
+// global memory, the backward needs no stored P:
+//   P_ij = exp(S_ij - L_i),  dV = P^T dO,  dP = dO V^T,  dS = P o (dP - D),
+//   dQ = sm_scale dS K,  dK = sm_scale dS^T Q.
+// dQ accumulates along key tiles and dK/dV along query tiles, so (as on that
+// page) the work is split into two passes that each recompute P:
+//   bwd_pre_kernel   D_i and L_i * log2(e) per query row into the workspace
+//                    (padded to whole 128-row tiles: D = 0, L = +inf)
+//   dkdv_kernel      one CTA per 128-key tile, loop over query tiles:
+//                    S^T = K Q_i^T, dP^T = V dO_i^T (TMEM), P^T and dS^T by
+//                    eight elementwise warps, dV += P^T dO_i, dK += dS^T Q_i
+//   dq_kernel        one CTA per 128-query tile, loop over key tiles:
+//                    S = Q K_j^T, dP = dO V_j^T, dS, dQ += dS K_j
+// P is exp2(c S - L log2 e) with c = sm_scale log2(e) ("Fused Attention 2":
+// exp2 with the scale folded by log2 e).  P^T and dS^T (dS) are rounded to the
+// input type and written back into the TMEM columns they were computed from,
+// where they are the A operand of the next tcgen05.mma.
+// Causal: only query/key tile pairs on or below the diagonal are visited; only
+// the diagonal tile is masked.
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <math_constants.h>
+
+namespace fa {
+namespace {
+
+constexpr int kT = 128;                  // rows per query / key tile
+constexpr int kChunk = 128 * 128;        // 128 rows x 64 columns x 2 bytes
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ const uint8_t* row_ptr(const void* base, int64_t sb, int64_t sh, int64_t ss, int b,
+                                                  int h, int r) {
+  return reinterpret_cast<const uint8_t*>(base) +
+         2 * (static_cast<int64_t>(b) * sb + static_cast<int64_t>(h) * sh + static_cast<int64_t>(r) * ss);
+}
+
+// 16-bit pair -> two fp32
+template <bool BF16>
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+  float2 f;
+  if constexpr (BF16) {
+    f.x = __uint_as_float(w << 16);
+    f.y = __uint_as_float(w & 0xffff0000u);
+  } else {
+    __half2 hh = *reinterpret_cast<__half2*>(&w);
+    f = __half22float2(hh);
+  }
+  return f;
+}
+
+// ---------------------------------------------------------------------------
+// D = rowsum(O o dO), L2 = LSE * log2(e), padded per (b, h) to Nqp rows
+// ---------------------------------------------------------------------------
+struct PreParams {
+  const void* o;
+  int64_t o_sb, o_sh, o_ss;
+  const void* dout;
+  int64_t d_sb, d_sh, d_ss;
+  const float* lse;
+  float* wsD;
+  float* wsL;
+  int B, H, Nq, Nqp, d;
+};
+
+template <bool BF16>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const PreParams p) {
+  const long long gid = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 3;
+  const int sub = threadIdx.x & 7;
+  const long long total = static_cast<long long>(p.B) * p.H * p.Nqp;
+  const bool active = gid < total;
+  const long long row = active ? gid : 0;
+  const int bh = static_cast<int>(row / p.Nqp);
+  const int q = static_cast<int>(row % p.Nqp);
+  const int b = bh / p.H;
+  const int h = bh % p.H;
+  const bool valid = active && q < p.Nq;
+  float acc = 0.f;
+  if (valid) {
+    const uint4* po = reinterpret_cast<const uint4*>(row_ptr(p.o, p.o_sb, p.o_sh, p.o_ss, b, h, q));
+    const uint4* pd = reinterpret_cast<const uint4*>(row_ptr(p.dout, p.d_sb, p.d_sh, p.d_ss, b, h, q));
+    for (int c = sub; c < p.d / 8; c += 8) {
+      const uint4 a = __ldg(po + c);
+      const uint4 g = __ldg(pd + c);
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+      const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 fa = unpack2<BF16>(aw[e]);
+        const float2 fg = unpack2<BF16>(gw[e]);
+        acc = fmaf(fa.x, fg.x, acc);
+        acc = fmaf(fa.y, fg.y, acc);
+      }
+    }
+  }
+  acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+  if (active && sub == 0) {
+    p.wsD[row] = valid ? acc : 0.f;
+    p.wsL[row] = valid ? p.lse[static_cast<long long>(bh) * p.Nq + q] * kLog2e : CUDART_INF_F;
+  }
+}
+
+// zero dK and dV when there are no queries
+template <int D>
+__global__ void zero_rows_kernel(void* x, int64_t sb, int64_t sh, int64_t ss, int B, int H, int N) {
+  const long long r = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (r >= static_cast<long long>(B) * H * N) return;
+  const int n = static_cast<int>(r % N);
+  const int bh = static_cast<int>(r / N);
+  uint4* dst = reinterpret_cast<uint4*>(const_cast<uint8_t*>(row_ptr(x, sb, sh, ss, bh / H, bh % H, n)));
+#pragma unroll
+  for (int c = 0; c < D / 8; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+}
+
+// ---------------------------------------------------------------------------
+// shared pieces of the two main kernels
+// ---------------------------------------------------------------------------
+template <int D>
+struct BwdCfg {
+  static constexpr int DCH = (D + 63) / 64;
+  static constexpr int TILE = DCH * kChunk;
+  static constexpr int THREADS = 320;   // 8 elementwise warps, producer, MMA
+  static constexpr int PROD_WARP = 8;
+  static constexpr int MMA_WARP = 9;
+  // dK/dV: K, V resident; ring of (Q_i, dO_i, L_i, D_i)
+  static constexpr int KV_NSTAGE = D <= 64 ? 4 : 2;
+  static constexpr int KV_STAGE = 2 * TILE + 2 * 512;
+  static constexpr int KV_SMEM = 1024 + 2 * TILE + KV_NSTAGE * KV_STAGE + 256;
+  // dQ: Q, dO resident; ring of (K_j, V_j)
+  static constexpr int Q_NSTAGE = D <= 64 ? 4 : 2;
+  static constexpr int Q_STAGE = 2 * TILE;
+  static constexpr int Q_SMEM = 1024 + 2 * TILE + Q_NSTAGE * Q_STAGE + 256;
+};
+
+// TMEM column of the A operand for K-step ks (16 elements) when the 16-bit
+// matrix was written by two warpgroups, each packing its 64 columns into the
+// first 32 columns of its own 64-column half.
+__device__ __forceinline__ uint32_t split_a_col(int ks) { return (ks >> 2) * 64 + (ks & 3) * 8; }
+
+// M = 128 x N = 128 x K = D, both operands K-major in 128B-swizzled tiles.
+template <int D>
+__device__ __forceinline__ void mma_nt(uint32_t d_tmem, uint32_t a_addr, uint32_t b_addr, uint32_t idesc) {
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    const uint32_t off = (ks >> 2) * kChunk + (ks & 3) * 32;
+    umma_ss(d_tmem, make_sdesc_sw128(a_addr + off, 16, 1024), make_sdesc_sw128(b_addr + off, 16, 1024), idesc,
+            ks > 0);
+  }
+}
+
+// D(128 x D) (+)= A(TMEM, 128 x 128) * B(128 x D, MN-major tile of 128 rows).
+__device__ __forceinline__ void mma_tn(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_addr, uint32_t idesc,
+                                       bool acc) {
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    umma_ts(d_tmem, a_tmem + split_a_col(ks), make_sdesc_sw128(b_addr + ks * 16 * 128, kChunk, 1024), idesc,
+            (acc || ks > 0) ? 1u : 0u);
+  }
+}
+
+struct MainParams {
+  int B, H, Nq, Nk, Nqp;
+  int causal;
+  float scale_log2;   // sm_scale * log2(e)
+  float sm_scale;
+  const float* wsD;
+  const float* wsL;
+  void* out0;         // dkdv: dV   dq: dQ
+  int64_t o0_sb, o0_sh, o0_ss;
+  void* out1;         // dkdv: dK
+  int64_t o1_sb, o1_sh, o1_ss;
+  int* err;
+};
+
+// Store 16 fp32 TMEM columns of this thread's row, times `scale`, as 16-bit.
+template <bool BF16>
+__device__ __forceinline__ void store16(uint8_t* dst, const uint32_t (&v)[16], float scale) {
+  uint4 w0, w1;
+  w0.x = pack2<BF16>(__uint_as_float(v[0]) * scale, __uint_as_float(v[1]) * scale);
+  w0.y = pack2<BF16>(__uint_as_float(v[2]) * scale, __uint_as_float(v[3]) * scale);
+  w0.z = pack2<BF16>(__uint_as_float(v[4]) * scale, __uint_as_float(v[5]) * scale);
+  w0.w = pack2<BF16>(__uint_as_float(v[6]) * scale, __uint_as_float(v[7]) * scale);
+  w1.x = pack2<BF16>(__uint_as_float(v[8]) * scale, __uint_as_float(v[9]) * scale);
+  w1.y = pack2<BF16>(__uint_as_float(v[10]) * scale, __uint_as_float(v[11]) * scale);
+  w1.z = pack2<BF16>(__uint_as_float(v[12]) * scale, __uint_as_float(v[13]) * scale);
+  w1.w = pack2<BF16>(__uint_as_float(v[14]) * scale, __uint_as_float(v[15]) * scale);
+  reinterpret_cast<uint4*>(dst)[0] = w0;
+  reinterpret_cast<uint4*>(dst)[1] = w1;
+}
+
+// ---------------------------------------------------------------------------
+// dK / dV: one CTA per (key tile, b, h)
+// ---------------------------------------------------------------------------
+// TMEM columns: [0,128) S^T -> P^T, [128,256) dP^T -> dS^T, [256,256+D) dV,
+// [384,384+D) dK.  Elementwise warps: warpgroup g = warp / 4 owns query
+// columns [64 g, 64 g + 64) of S^T / dP^T; warp % 4 selects the 32 key rows.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
+    dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                const MainParams p) {
+  using C = BwdCfg<D>;
+  constexpr int NS = C::KV_NSTAGE;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sK = smem;
+  uint8_t* sV = smem + C::TILE;
+  uint8_t* sStage = smem + 2 * C::TILE;   // per stage: Q, dO, L[128], D[128]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + NS * C::KV_STAGE);
+  uint64_t* bar_kv = bars;            // K, V loaded
+  uint64_t* bar_full = bars + 1;      // [NS]
+  uint64_t* bar_empty = bar_full + NS;
+  uint64_t* bar_s = bar_empty + NS;   // S^T ready
+  uint64_t* bar_dp = bar_s + 1;       // dP^T ready
+  uint64_t* bar_pt = bar_dp + 1;      // P^T written (256 arrivals)
+  uint64_t* bar_ds = bar_pt + 1;      // dS^T written (256 arrivals)
+  uint64_t* bar_acc = bar_ds + 1;     // all MMAs done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_acc + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int BH = p.B * p.H;
+  // Heaviest key tiles first (for causal the first key tile sees every query).
+  const int kt = static_cast<int>(blockIdx.x / BH);
+  const int bh = static_cast<int>(blockIdx.x % BH);
+  const int b = bh / p.H;
+  const int h = bh % p.H;
+  const int k0 = kt * kT;
+  const int nqt = (p.Nq + kT - 1) / kT;
+  const int i_first = p.causal ? min(k0 / kT, nqt) : 0;
+  const int n_it = nqt - i_first;   // query tiles this key tile meets
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_kv, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
+    mbar_init(bar_s, 1);
+    mbar_init(bar_dp, 1);
+    mbar_init(bar_pt, 256);
+    mbar_init(bar_ds, 256);
+    mbar_init(bar_acc, 1);
+    fence_mbar_init();
+  }
+  if (warp == C::MMA_WARP) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == C::PROD_WARP) {
+    if (lane == 0 && n_it > 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmdO);
+      mbar_arrive_expect_tx(bar_kv, 2 * C::TILE);
+      for (int c = 0; c < C::DCH; ++c) {
+        tma_load_4d(sK + c * kChunk, &tmK, bar_kv, c * 64, k0, h, b);
+        tma_load_4d(sV + c * kChunk, &tmV, bar_kv, c * 64, k0, h, b);
+      }
+      for (int it = 0; it < n_it; ++it) {
+        const int s = it % NS;
+        const int use = it / NS;
+        if (use > 0) mbar_wait(&bar_empty[s], (use - 1) & 1, p.err, 21);
+        uint8_t* st = sStage + s * C::KV_STAGE;
+        const int q0 = (i_first + it) * kT;
+        mbar_arrive_expect_tx(&bar_full[s], 2 * C::TILE + 1024);
+        for (int c = 0; c < C::DCH; ++c) {
+          tma_load_4d(st + c * kChunk, &tmQ, &bar_full[s], c * 64, q0, h, b);
+          tma_load_4d(st + C::TILE + c * kChunk, &tmdO, &bar_full[s], c * 64, q0, h, b);
+        }
+        const int64_t off = static_cast<int64_t>(bh) * p.Nqp + q0;
+        bulk_load(st + 2 * C::TILE, p.wsL + off, 512, &bar_full[s]);
+        bulk_load(st + 2 * C::TILE + 512, p.wsD + off, 512, &bar_full[s]);
+      }
+      for (int it = max(0, n_it - NS); it < n_it; ++it) mbar_wait_drain(&bar_full[it % NS], (it / NS) & 1);
+      mbar_wait_drain(bar_kv, 0);
+    }
+  } else if (warp == C::MMA_WARP) {
+    if (lane == 0 && n_it > 0) {
+      constexpr uint32_t idesc_nt = make_idesc_f16(BF16, kT, kT, false, false);
+      constexpr uint32_t idesc_tn = make_idesc_f16(BF16, kT, D, false, true);
+      const uint32_t sk = smem_u32(sK);
+      const uint32_t sv = smem_u32(sV);
+      const uint32_t sst = smem_u32(sStage);
+      const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
+      mbar_wait(bar_kv, 0, p.err, 22);
+      mbar_wait(&bar_full[0], 0, p.err, 23);
+      tc_fence_after();
+      mma_nt<D>(tS, sk, sst, idesc_nt);                 // S^T_0 = K Q_0^T
+      umma_commit(bar_s);
+      mma_nt<D>(tdP, sv, sst + C::TILE, idesc_nt);      // dP^T_0 = V dO_0^T
+      umma_commit(bar_dp);
+      for (int it = 0; it < n_it; ++it) {
+        const int s = it % NS;
+        const uint32_t sq = sst + s * C::KV_STAGE;
+        const uint32_t sdo = sq + C::TILE;
+        mbar_wait(bar_pt, it & 1, p.err, 24);
+        tc_fence_after();
+        mma_tn(tdV, tS, sdo, idesc_tn, it > 0);          // dV += P^T dO_i
+        if (it + 1 < n_it) {
+          const int s1 = (it + 1) % NS;
+          mbar_wait(&bar_full[s1], ((it + 1) / NS) & 1, p.err, 25);
+          tc_fence_after();
+          mma_nt<D>(tS, sk, sst + s1 * C::KV_STAGE, idesc_nt);   // S^T_{i+1}
+          umma_commit(bar_s);
+        }
+        mbar_wait(bar_ds, it & 1, p.err, 26);
+        tc_fence_after();
+        mma_tn(tdK, tdP, sq, idesc_tn, it > 0);          // dK += dS^T Q_i
+        umma_commit(&bar_empty[s]);
+        if (it + 1 < n_it) {
+          const int s1 = (it + 1) % NS;
+          mma_nt<D>(tdP, sv, sst + s1 * C::KV_STAGE + C::TILE, idesc_nt);   // dP^T_{i+1}
+          umma_commit(bar_dp);
+        }
+      }
+      umma_commit(bar_acc);
+      mbar_wait_drain(bar_acc, 0);
+    }
+  } else {
+    // ------------------------------------------------------- elementwise
+    const int g = warp >> 2;             // query-column half
+    const int quad = warp & 3;
+    const int krow = k0 + quad * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t tS = tmem + lane_off + g * 64;
+    const uint32_t tdP = tmem + lane_off + 128 + g * 64;
+    const float cs = p.scale_log2;
+
+    for (int it = 0; it < n_it; ++it) {
+      const int s = it % NS;
+      const float* sL = reinterpret_cast<const float*>(sStage + s * C::KV_STAGE + 2 * C::TILE) + g * 64;
+      const float* sD = sL + 128;
+      const int q0 = (i_first + it) * kT + g * 64;   // first query of this half
+      const bool diag = p.causal && (q0 < k0 + kT - 1);   // some column q < some row k
+
+      mbar_wait(bar_s, it & 1, p.err, 27);
+      // L/D of this stage are in shared memory once the stage's TMA landed;
+      // S^T_i completing implies the stage was waited on by the MMA thread.
+      mbar_wait(&bar_full[s], (it / NS) & 1, p.err, 28);
+      tc_fence_after();
+      float pt[64];
+      {
+        uint32_t r[32];
+        tmem_ld32(tS, r);
+        uint32_t r2[32];
+        tmem_ld32(tS + 32, r2);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          pt[e] = __uint_as_float(r[e]);
+          pt[32 + e] = __uint_as_float(r2[e]);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 64; ++e) pt[e] = ex2_approx(fmaf(pt[e], cs, -sL[e]));
+      if (diag) {
+#pragma unroll
+        for (int e = 0; e < 64; ++e)
+          if (q0 + e < krow) pt[e] = 0.f;
+      }
+      {
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) pk[e] = pack2<BF16>(pt[2 * e], pt[2 * e + 1]);
+        tmem_st16(tS, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+        tmem_st16(tS + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_pt);
+
+      mbar_wait(bar_dp, it & 1, p.err, 29);
+      tc_fence_after();
+      {
+        uint32_t r[32];
+        tmem_ld32(tdP, r);
+        uint32_t r2[32];
+        tmem_ld32(tdP + 32, r2);
+        tmem_wait_ld();
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float a0 = pt[2 * e] * (__uint_as_float(r[2 * e]) - sD[2 * e]);
+          const float a1 = pt[2 * e + 1] * (__uint_as_float(r[2 * e + 1]) - sD[2 * e + 1]);
+          pk[e] = pack2<BF16>(a0, a1);
+          const float b0 = pt[32 + 2 * e] * (__uint_as_float(r2[2 * e]) - sD[32 + 2 * e]);
+          const float b1 = pt[32 + 2 * e + 1] * (__uint_as_float(r2[2 * e + 1]) - sD[32 + 2 * e + 1]);
+          pk[16 + e] = pack2<BF16>(b0, b1);
+        }
+        tmem_st16(tdP, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+        tmem_st16(tdP + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_ds);
+    }
+
+    // epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK * sm_scale
+    if (n_it > 0) {
+      mbar_wait(bar_acc, 0, p.err, 30);
+      tc_fence_after();
+    }
+    const bool valid = krow < p.Nk;
+    void* outp = g == 0 ? p.out0 : p.out1;
+    const int64_t sb = g == 0 ? p.o0_sb : p.o1_sb;
+    const int64_t sh = g == 0 ? p.o0_sh : p.o1_sh;
+    const int64_t ss = g == 0 ? p.o0_ss : p.o1_ss;
+    const float scale = g == 0 ? 1.f : p.sm_scale;
+    uint8_t* dst = const_cast<uint8_t*>(row_ptr(outp, sb, sh, ss, b, h, krow));
+    const uint32_t tacc = tmem + lane_off + (g == 0 ? 256 : 384);
+#pragma unroll
+    for (int c = 0; c < D / 16; ++c) {
+      uint32_t v[16];
+      if (n_it > 0) {
+        tmem_ld16(tacc + c * 16, v);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = 0u;
+      }
+      if (valid) store16<BF16>(dst + c * 32, v, scale);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// dQ: one CTA per (query tile, b, h)
+// ---------------------------------------------------------------------------
+// TMEM columns: [0,128) S, [128,256) dP -> dS, [256,256+D) dQ.  Elementwise
+// warps: warpgroup g owns key columns [64 g, 64 g + 64); warp % 4 selects
+// the 32 query rows.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
+    dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+              const MainParams p) {
+  using C = BwdCfg<D>;
+  constexpr int NS = C::Q_NSTAGE;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sdO = smem + C::TILE;
+  uint8_t* sStage = smem + 2 * C::TILE;   // per stage: K_j, V_j
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + NS * C::Q_STAGE);
+  uint64_t* bar_q = bars;
+  uint64_t* bar_full = bars + 1;
+  uint64_t* bar_empty = bar_full + NS;
+  uint64_t* bar_s = bar_empty + NS;
+  uint64_t* bar_dp = bar_s + 1;
+  uint64_t* bar_sfree = bar_dp + 1;   // S read into registers (256 arrivals)
+  uint64_t* bar_ds = bar_sfree + 1;   // dS written (256 arrivals)
+  uint64_t* bar_acc = bar_ds + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_acc + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int BH = p.B * p.H;
+  const int nqt = (p.Nq + kT - 1) / kT;
+  // Heaviest query tiles first (for causal the last query tile sees every key).
+  const int qt = nqt - 1 - static_cast<int>(blockIdx.x / BH);
+  const int bh = static_cast<int>(blockIdx.x % BH);
+  const int b = bh / p.H;
+  const int h = bh % p.H;
+  const int q0 = qt * kT;
+  int n_jt = (p.Nk + kT - 1) / kT;
+  if (p.causal) n_jt = min(n_jt, min(q0 + kT - 1, p.Nq - 1) / kT + 1);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_q, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
+    mbar_init(bar_s, 1);
+    mbar_init(bar_dp, 1);
+    mbar_init(bar_sfree, 256);
+    mbar_init(bar_ds, 256);
+    mbar_init(bar_acc, 1);
+    fence_mbar_init();
+  }
+  if (warp == C::MMA_WARP) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == C::PROD_WARP) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      mbar_arrive_expect_tx(bar_q, 2 * C::TILE);
+      for (int c = 0; c < C::DCH; ++c) {
+        tma_load_4d(sQ + c * kChunk, &tmQ, bar_q, c * 64, q0, h, b);
+        tma_load_4d(sdO + c * kChunk, &tmdO, bar_q, c * 64, q0, h, b);
+      }
+      for (int jt = 0; jt < n_jt; ++jt) {
+        const int s = jt % NS;
+        const int use = jt / NS;
+        if (use > 0) mbar_wait(&bar_empty[s], (use - 1) & 1, p.err, 41);
+        uint8_t* st = sStage + s * C::Q_STAGE;
+        mbar_arrive_expect_tx(&bar_full[s], 2 * C::TILE);
+        for (int c = 0; c < C::DCH; ++c) {
+          tma_load_4d(st + c * kChunk, &tmK, &bar_full[s], c * 64, jt * kT, h, b);
+          tma_load_4d(st + C::TILE + c * kChunk, &tmV, &bar_full[s], c * 64, jt * kT, h, b);
+        }
+      }
+      for (int jt = max(0, n_jt - NS); jt < n_jt; ++jt) mbar_wait_drain(&bar_full[jt % NS], (jt / NS) & 1);
+      mbar_wait_drain(bar_q, 0);
+    }
+  } else if (warp == C::MMA_WARP) {
+    if (lane == 0 && n_jt > 0) {
+      constexpr uint32_t idesc_nt = make_idesc_f16(BF16, kT, kT, false, false);
+      constexpr uint32_t idesc_tn = make_idesc_f16(BF16, kT, D, false, true);
+      const uint32_t sq = smem_u32(sQ);
+      const uint32_t sdo = smem_u32(sdO);
+      const uint32_t sst = smem_u32(sStage);
+      const uint32_t tS = tmem, tdP = tmem + 128, tdQ = tmem + 256;
+      mbar_wait(bar_q, 0, p.err, 42);
+      mbar_wait(&bar_full[0], 0, p.err, 43);
+      tc_fence_after();
+      mma_nt<D>(tS, sq, sst, idesc_nt);                   // S_0 = Q K_0^T
+      umma_commit(bar_s);
+      mma_nt<D>(tdP, sdo, sst + C::TILE, idesc_nt);       // dP_0 = dO V_0^T
+      umma_commit(bar_dp);
+      for (int jt = 0; jt < n_jt; ++jt) {
+        const int s = jt % NS;
+        const uint32_t sk = sst + s * C::Q_STAGE;
+        if (jt + 1 < n_jt) {
+          const int s1 = (jt + 1) % NS;
+          mbar_wait(&bar_full[s1], ((jt + 1) / NS) & 1, p.err, 44);
+          mbar_wait(bar_sfree, jt & 1, p.err, 45);
+          tc_fence_after();
+          mma_nt<D>(tS, sq, sst + s1 * C::Q_STAGE, idesc_nt);   // S_{j+1}
+          umma_commit(bar_s);
+        }
+        mbar_wait(bar_ds, jt & 1, p.err, 46);
+        tc_fence_after();
+        mma_tn(tdQ, tdP, sk, idesc_tn, jt > 0);           // dQ += dS K_j
+        umma_commit(&bar_empty[s]);
+        if (jt + 1 < n_jt) {
+          const int s1 = (jt + 1) % NS;
+          mma_nt<D>(tdP, sdo, sst + s1 * C::Q_STAGE + C::TILE, idesc_nt);   // dP_{j+1}
+          umma_commit(bar_dp);
+        }
+      }
+      umma_commit(bar_acc);
+      mbar_wait_drain(bar_acc, 0);
+    }
+  } else {
+    const int g = warp >> 2;
+    const int quad = warp & 3;
+    const int qrow = q0 + quad * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t tS = tmem + lane_off + g * 64;
+    const uint32_t tdP = tmem + lane_off + 128 + g * 64;
+    const float cs = p.scale_log2;
+    const int64_t wrow = static_cast<int64_t>(bh) * p.Nqp + qrow;
+    const float Lr = p.wsL[wrow];   // +inf on padded rows
+    const float Dr = p.wsD[wrow];
+
+    for (int jt = 0; jt < n_jt; ++jt) {
+      const int kb = jt * kT + g * 64;   // first key of this half
+      const bool need_mask = (kb + 64 > p.Nk) || (p.causal && kb + 63 > q0);
+      const int lim = p.causal ? min(p.Nk, qrow + 1) : p.Nk;
+
+      mbar_wait(bar_s, jt & 1, p.err, 47);
+      tc_fence_after();
+      float pr[64];
+      {
+        uint32_t r[32];
+        tmem_ld32(tS, r);
+        uint32_t r2[32];
+        tmem_ld32(tS + 32, r2);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          pr[e] = __uint_as_float(r[e]);
+          pr[32 + e] = __uint_as_float(r2[e]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar_sfree);
+#pragma unroll
+      for (int e = 0; e < 64; ++e) pr[e] = ex2_approx(fmaf(pr[e], cs, -Lr));
+      if (need_mask) {
+#pragma unroll
+        for (int e = 0; e < 64; ++e)
+          if (kb + e >= lim) pr[e] = 0.f;
+      }
+      mbar_wait(bar_dp, jt & 1, p.err, 48);
+      tc_fence_after();
+      {
+        uint32_t r[32];
+        tmem_ld32(tdP, r);
+        uint32_t r2[32];
+        tmem_ld32(tdP + 32, r2);
+        tmem_wait_ld();
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          pk[e] = pack2<BF16>(pr[2 * e] * (__uint_as_float(r[2 * e]) - Dr),
+                              pr[2 * e + 1] * (__uint_as_float(r[2 * e + 1]) - Dr));
+          pk[16 + e] = pack2<BF16>(pr[32 + 2 * e] * (__uint_as_float(r2[2 * e]) - Dr),
+                                   pr[32 + 2 * e + 1] * (__uint_as_float(r2[2 * e + 1]) - Dr));
+        }
+        tmem_st16(tdP, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+        tmem_st16(tdP + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_ds);
+    }
+
+    // epilogue: dQ * sm_scale; 16-column chunks alternate between warpgroups
+    if (n_jt > 0) {
+      mbar_wait(bar_acc, 0, p.err, 49);
+      tc_fence_after();
+    }
+    const bool valid = qrow < p.Nq;
+    uint8_t* dst = const_cast<uint8_t*>(row_ptr(p.out0, p.o0_sb, p.o0_sh, p.o0_ss, b, h, qrow));
+    const uint32_t tacc = tmem + lane_off + 256;
+#pragma unroll
+    for (int c = 0; c < D / 16; ++c) {
+      if ((c & 1) != g) continue;
+      uint32_t v[16];
+      if (n_jt > 0) {
+        tmem_ld16(tacc + c * 16, v);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = 0u;
+      }
+      if (valid) store16<BF16>(dst + c * 32, v, p.sm_scale);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool BF16>
+cudaError_t launch_bwd_t(const BwdArgs& a, int phase, cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  const int BH = a.B * a.H;
+  cudaError_t e;
+  if (a.Nq == 0) {
+    if (phase == 1 || phase == 3) return cudaSuccess;
+    const long long rows = static_cast<long long>(BH) * a.Nk;
+    const unsigned blocks = static_cast<unsigned>((rows + 255) / 256);
+    zero_rows_kernel<D><<<blocks, 256, 0, stream>>>(const_cast<void*>(a.dk.ptr), a.dk.sb, a.dk.sh, a.dk.ss, a.B,
+                                                     a.H, a.Nk);
+    zero_rows_kernel<D><<<blocks, 256, 0, stream>>>(const_cast<void*>(a.dv.ptr), a.dv.sb, a.dv.sh, a.dv.ss, a.B,
+                                                     a.H, a.Nk);
+    return cudaGetLastError();
+  }
+  const int Nqp = nq_pad(a.Nq);
+  float* wsD = a.ws;
+  float* wsL = a.ws + static_cast<size_t>(BH) * Nqp;
+
+  PreParams pp;
+  pp.o = a.o.ptr;
+  pp.o_sb = a.o.sb;
+  pp.o_sh = a.o.sh;
+  pp.o_ss = a.o.ss;
+  pp.dout = a.dout.ptr;
+  pp.d_sb = a.dout.sb;
+  pp.d_sh = a.dout.sh;
+  pp.d_ss = a.dout.ss;
+  pp.lse = a.lse;
+  pp.wsD = wsD;
+  pp.wsL = wsL;
+  pp.B = a.B;
+  pp.H = a.H;
+  pp.Nq = a.Nq;
+  pp.Nqp = Nqp;
+  pp.d = D;
+  if (phase == 0 || phase == 1) {
+    const long long rows = static_cast<long long>(BH) * Nqp;
+    const long long blocks = (rows * 8 + 255) / 256;
+    bwd_pre_kernel<BF16><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(pp);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+
+  if (phase == 1) return cudaSuccess;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_tile_map(&tq, a.q, D, a.Nq, a.H, a.B, BF16) || !make_tile_map(&tk, a.k, D, a.Nk, a.H, a.B, BF16) ||
+      !make_tile_map(&tv, a.v, D, a.Nk, a.H, a.B, BF16) || !make_tile_map(&tdo, a.dout, D, a.Nq, a.H, a.B, BF16))
+    return cudaErrorInvalidValue;
+
+  MainParams mp;
+  mp.B = a.B;
+  mp.H = a.H;
+  mp.Nq = a.Nq;
+  mp.Nk = a.Nk;
+  mp.Nqp = Nqp;
+  mp.causal = a.causal;
+  mp.scale_log2 = a.sm_scale * kLog2e;
+  mp.sm_scale = a.sm_scale;
+  mp.wsD = wsD;
+  mp.wsL = wsL;
+  mp.err = a.err;
+
+  // dK, dV
+  mp.out0 = const_cast<void*>(a.dv.ptr);
+  mp.o0_sb = a.dv.sb;
+  mp.o0_sh = a.dv.sh;
+  mp.o0_ss = a.dv.ss;
+  mp.out1 = const_cast<void*>(a.dk.ptr);
+  mp.o1_sb = a.dk.sb;
+  mp.o1_sh = a.dk.sh;
+  mp.o1_ss = a.dk.ss;
+  if (phase == 0 || phase == 2) {
+    auto kern = dkdv_kernel<D, BF16>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::KV_SMEM);
+    if (e != cudaSuccess) return e;
+    const long long blocks = static_cast<long long>((a.Nk + kT - 1) / kT) * BH;
+    kern<<<static_cast<unsigned>(blocks), C::THREADS, C::KV_SMEM, stream>>>(tq, tk, tv, tdo, mp);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  // dQ
+  mp.out0 = const_cast<void*>(a.dq.ptr);
+  mp.o0_sb = a.dq.sb;
+  mp.o0_sh = a.dq.sh;
+  mp.o0_ss = a.dq.ss;
+  mp.out1 = nullptr;
+  if (phase == 0 || phase == 3) {
+    auto kern = dq_kernel<D, BF16>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::Q_SMEM);
+    if (e != cudaSuccess) return e;
+    const long long blocks = static_cast<long long>((a.Nq + kT - 1) / kT) * BH;
+    kern<<<static_cast<unsigned>(blocks), C::THREADS, C::Q_SMEM, stream>>>(tq, tk, tv, tdo, mp);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const BwdArgs& a, int phase, cudaStream_t stream) {
+  switch (a.d) {
+    case 64: return a.bf16 ? launch_bwd_t<64, true>(a, phase, stream) : launch_bwd_t<64, false>(a, phase, stream);
+    case 80: return a.bf16 ? launch_bwd_t<80, true>(a, phase, stream) : launch_bwd_t<80, false>(a, phase, stream);
+    case 128:
+      return a.bf16 ? launch_bwd_t<128, true>(a, phase, stream) : launch_bwd_t<128, false>(a, phase, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace fa

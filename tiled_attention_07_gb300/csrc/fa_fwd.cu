@@ -1,0 +1,424 @@
+// fa_fwd.cu -- FlashAttention-2 forward for sm_103a (tcgen05 + TMA).
+//
+// Computes O = softmax(sm_scale * Q K^T [+ causal mask]) V and the per-row
+// natural-log LSE with the online-softmax recurrences of "[CS336] Assignment 2:
+// Systems", "FlashAttention V2 / Forward Pass" (running max m, running sum l,
+// one query tile against all key tiles, no tiling over d), evaluated in the
+// exp2 domain with sm_scale folded by log2(e) as in "Understanding Triton
+// Tutorials Part 2", "Fused Attention 2" (_attn_fwd_inner: qk_scale =
+// sm_scale * 1.44269504, p = exp2(qk - m), alpha = exp2(m_old - m_new)), and the
+// delayed normalisation of FA-2 (O divided by the final l only).
+//
+// GB300 design (one CTA = two 128-row query tiles of one (b, h)):
+//   warps 0-3  softmax / correction / epilogue of query tile 0 (one row each)
+//   warps 4-7  the same for query tile 1
+//   warp  8    TMA producer: Q tiles once, then K_j, V_j through an
+//              mbarrier ring of NSTAGE shared-memory slots
+//   warp  9    TMEM allocator and single-thread tcgen05.mma issuer
+// Tensor memory (512 columns x 128 lanes): S_t at column 128*t (fp32 scores,
+// overwritten in place by the 16-bit P_t that feeds the PV MMA as its A
+// operand), O_t at column 256 + 128*t (fp32 accumulator).  The MMA thread
+// ping-pongs the two tiles: while tile 0's softmax runs on S_0 the tensor
+// cores compute PV and the next S of tile 1, and the other way round.
+// O is rescaled in TMEM only when a row's running max grows by more than
+// 2^8 (the stale max stays exact because l uses the same max).
+// Causal: tiles above the diagonal are never loaded or computed; only the
+// diagonal tile and the ragged key tail are masked.
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <math_constants.h>
+
+namespace fa {
+namespace {
+
+constexpr int kBM = 128;          // query rows per tile
+constexpr int kBN = 128;          // keys per tile
+constexpr int kNQT = 2;           // query tiles per CTA
+constexpr int kChunkBytes = 128 * 128;  // 128 rows x 64 columns x 2 bytes
+constexpr float kRescaleLog2 = 8.0f;
+
+template <int D>
+struct FwdCfg {
+  static constexpr int DCH = (D + 63) / 64;            // 64-column chunks per row
+  static constexpr int TILE = DCH * kChunkBytes;        // one 128-row tile
+  static constexpr int NSTAGE = D <= 64 ? 8 : 4;        // K/V ring depth
+  static constexpr int SMEM_DATA = kNQT * TILE + NSTAGE * TILE;
+  static constexpr int NBARS = kNQT + 2 * NSTAGE + 3 * kNQT + 1;
+  static constexpr int SMEM = 1024 + SMEM_DATA + NBARS * 8 + 16;
+  static constexpr int THREADS = kNQT * 128 + 64;
+  static constexpr int PROD_WARP = kNQT * 4;
+  static constexpr int MMA_WARP = kNQT * 4 + 1;
+};
+
+struct FwdParams {
+  int B, H, Nq, Nk;
+  int n_pairs;          // ceil(Nq / 256)
+  int causal;
+  float scale_log2;     // sm_scale * log2(e)
+  void* o;
+  int64_t o_sb, o_sh, o_ss;
+  float* lse;
+  int* err;
+};
+
+// Number of key tiles query tile t (rows r0 .. r0+127) needs.
+__device__ __forceinline__ int key_tiles(int r0, int Nq, int Nk, int causal) {
+  if (r0 >= Nq) return 0;
+  int n = (Nk + kBN - 1) / kBN;
+  if (causal) {
+    const int last = min(r0 + kBM - 1, Nq - 1);
+    n = min(n, last / kBN + 1);
+  }
+  return n;
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sKV = smem + kNQT * C::TILE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + C::NSTAGE * C::TILE);
+  uint64_t* bar_q = bars;                           // [kNQT]
+  uint64_t* bar_full = bar_q + kNQT;                // [NSTAGE]
+  uint64_t* bar_empty = bar_full + C::NSTAGE;       // [NSTAGE]
+  uint64_t* bar_s = bar_empty + C::NSTAGE;          // [kNQT] S_t ready
+  uint64_t* bar_p = bar_s + kNQT;                   // [kNQT] P_t written (128 arrivals)
+  uint64_t* bar_o = bar_p + kNQT;                   // [kNQT] PV_t complete
+  uint64_t* bar_drain = bar_o + kNQT;               // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_drain + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // Work decode: heaviest query-tile pairs first (longest-processing-time
+  // order for causal), all (b, h) of one pair index next to each other.
+  const int BH = p.B * p.H;
+  const int lin = blockIdx.x;
+  const int pair = p.n_pairs - 1 - lin / BH;
+  const int bh = lin % BH;
+  const int b = bh / p.H;
+  const int h = bh % p.H;
+  const int q0 = pair * (kNQT * kBM);
+
+  int nkt[kNQT];
+  int n_max = 0;
+#pragma unroll
+  for (int t = 0; t < kNQT; ++t) {
+    nkt[t] = key_tiles(q0 + t * kBM, p.Nq, p.Nk, p.causal);
+    n_max = max(n_max, nkt[t]);
+  }
+
+  if (threadIdx.x == 0) {
+    for (int t = 0; t < kNQT; ++t) {
+      mbar_init(&bar_q[t], 1);
+      mbar_init(&bar_s[t], 1);
+      mbar_init(&bar_p[t], 128);
+      mbar_init(&bar_o[t], 1);
+    }
+    for (int s = 0; s < C::NSTAGE; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
+    mbar_init(bar_drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == C::MMA_WARP) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == C::PROD_WARP) {
+    // ------------------------------------------------------------------ TMA
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+#pragma unroll
+      for (int t = 0; t < kNQT; ++t) {
+        if (nkt[t] == 0) continue;
+        mbar_arrive_expect_tx(&bar_q[t], C::TILE);
+        for (int c = 0; c < C::DCH; ++c)
+          tma_load_4d(sQ + t * C::TILE + c * kChunkBytes, &tmQ, &bar_q[t], c * 64, q0 + t * kBM, h, b);
+      }
+      // K_0, V_0, K_1, V_1, ... : the order the MMA thread consumes them in.
+      const int nfill = 2 * n_max;
+      for (int f = 0; f < nfill; ++f) {
+        const int s = f % C::NSTAGE;
+        const int use = f / C::NSTAGE;
+        if (use > 0) mbar_wait(&bar_empty[s], (use - 1) & 1, p.err, 1);
+        mbar_arrive_expect_tx(&bar_full[s], C::TILE);
+        const int j = f >> 1;
+        const CUtensorMap* map = (f & 1) ? &tmV : &tmK;
+        for (int c = 0; c < C::DCH; ++c)
+          tma_load_4d(sKV + s * C::TILE + c * kChunkBytes, map, &bar_full[s], c * 64, j * kBN, h, b);
+      }
+      // Drain: the last fill of every slot has landed before the CTA exits.
+      for (int f = max(0, nfill - C::NSTAGE); f < nfill; ++f)
+        mbar_wait_drain(&bar_full[f % C::NSTAGE], (f / C::NSTAGE) & 1);
+#pragma unroll
+      for (int t = 0; t < kNQT; ++t)
+        if (nkt[t] > 0) mbar_wait_drain(&bar_q[t], 0);
+    }
+  } else if (warp == C::MMA_WARP) {
+    // ------------------------------------------------------------------ MMA
+    if (lane == 0 && n_max > 0) {
+      constexpr uint32_t idesc_s = make_idesc_f16(BF16, kBM, kBN, false, false);
+      constexpr uint32_t idesc_o = make_idesc_f16(BF16, kBM, D, false, true);
+      const uint32_t sq_addr = smem_u32(sQ);
+      const uint32_t skv_addr = smem_u32(sKV);
+
+      auto issue_s = [&](int t, int slot) {
+        // S_t = Q_t K^T : M = 128 queries, N = 128 keys, K = D (16 per MMA).
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * kChunkBytes + (ks & 3) * 32;
+          const uint64_t ad = make_sdesc_sw128(sq_addr + t * C::TILE + off, 16, 1024);
+          const uint64_t bd = make_sdesc_sw128(skv_addr + slot * C::TILE + off, 16, 1024);
+          umma_ss(tmem + t * 128, ad, bd, idesc_s, ks > 0);
+        }
+      };
+      auto issue_pv = [&](int t, int slot, bool acc) {
+        // O_t += P_t V : M = 128 queries, N = D, K = 128 keys (16 per MMA);
+        // P_t (16-bit, two per column) sits in TMEM columns [128 t, 128 t + 64).
+#pragma unroll
+        for (int ks = 0; ks < kBN / 16; ++ks) {
+          const uint64_t bd = make_sdesc_sw128(skv_addr + slot * C::TILE + ks * 16 * 128, kChunkBytes, 1024);
+          umma_ts(tmem + 256 + t * 128, tmem + t * 128 + ks * 8, bd, idesc_o, (acc || ks > 0) ? 1u : 0u);
+        }
+      };
+
+#pragma unroll
+      for (int t = 0; t < kNQT; ++t)
+        if (nkt[t] > 0) mbar_wait(&bar_q[t], 0, p.err, 2);
+      tc_fence_after();
+
+      // Prologue: S_t,0 for every tile.
+      {
+        const int f = 0;
+        mbar_wait(&bar_full[f % C::NSTAGE], (f / C::NSTAGE) & 1, p.err, 3);
+        tc_fence_after();
+#pragma unroll
+        for (int t = 0; t < kNQT; ++t)
+          if (nkt[t] > 0) {
+            issue_s(t, f % C::NSTAGE);
+            umma_commit(&bar_s[t]);
+          }
+        umma_commit(&bar_empty[f % C::NSTAGE]);
+      }
+      for (int j = 0; j < n_max; ++j) {
+        const int fv = 2 * j + 1;            // fill index of V_j
+        const int fk = 2 * j + 2;            // fill index of K_{j+1}
+        mbar_wait(&bar_full[fv % C::NSTAGE], (fv / C::NSTAGE) & 1, p.err, 4);
+        bool k_ready = false;
+#pragma unroll
+        for (int t = 0; t < kNQT; ++t) {
+          if (j >= nkt[t]) continue;
+          mbar_wait(&bar_p[t], j & 1, p.err, 5);
+          tc_fence_after();
+          issue_pv(t, fv % C::NSTAGE, j > 0);
+          umma_commit(&bar_o[t]);
+          if (j + 1 < nkt[t]) {
+            if (!k_ready) {
+              mbar_wait(&bar_full[fk % C::NSTAGE], (fk / C::NSTAGE) & 1, p.err, 6);
+              tc_fence_after();
+              k_ready = true;
+            }
+            issue_s(t, fk % C::NSTAGE);
+            umma_commit(&bar_s[t]);
+          }
+        }
+        umma_commit(&bar_empty[fv % C::NSTAGE]);
+        if (j + 1 < n_max) {
+          if (!k_ready) {
+            // No tile uses K_{j+1}; only possible when tiles end early. Keep
+            // the ring in step with the producer.
+            mbar_wait(&bar_full[fk % C::NSTAGE], (fk / C::NSTAGE) & 1, p.err, 7);
+          }
+          umma_commit(&bar_empty[fk % C::NSTAGE]);
+        }
+      }
+      // Drain: every MMA has completed before TMEM is released.
+      umma_commit(bar_drain);
+      mbar_wait_drain(bar_drain, 0);
+    }
+  } else {
+    // ------------------------------------------------- softmax / epilogue
+    const int t = warp >> 2;
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const int r0 = q0 + t * kBM;
+    const int qrow = r0 + row;
+    const int n = key_tiles(r0, p.Nq, p.Nk, p.causal);
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t tS = tmem + lane_off + t * 128;
+    const uint32_t tO = tmem + lane_off + 256 + t * 128;
+    const float cs = p.scale_log2;
+
+    float m = -CUDART_INF_F;  // running max of the scaled scores (log2 domain)
+    float l = 0.f;            // running sum of exp2(score - m)
+
+    for (int j = 0; j < n; ++j) {
+      mbar_wait(&bar_s[t], j & 1, p.err, 8);
+      if (j > 0) mbar_wait(&bar_o[t], (j - 1) & 1, p.err, 9);
+      tc_fence_after();
+
+      float s[kBN];
+#pragma unroll
+      for (int i = 0; i < kBN / 32; ++i) {
+        uint32_t r[32];
+        tmem_ld32(tS + i * 32, r);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) s[i * 32 + e] = __uint_as_float(r[e]);
+      }
+      tmem_wait_ld();
+
+      const int kbase = j * kBN;
+      const bool tail = kbase + kBN > p.Nk;
+      const bool diag = p.causal && (kbase + kBN - 1 > r0);
+      if (tail || diag) {
+        const int lim = p.causal ? min(p.Nk, qrow + 1) : p.Nk;  // keys < lim are visible
+#pragma unroll
+        for (int c = 0; c < kBN; ++c)
+          if (kbase + c >= lim) s[c] = -CUDART_INF_F;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
+      const float m_tile = mx * cs;
+
+      if (j == 0) {
+        m = m_tile;
+      } else {
+        const bool need = m_tile > m + kRescaleLog2;
+        if (__any_sync(0xffffffffu, need)) {
+          const float m_new = need ? m_tile : m;
+          const float alpha = ex2_approx(m - m_new);
+          m = m_new;
+          l *= alpha;
+#pragma unroll
+          for (int c = 0; c < D / 16; ++c) {
+            uint32_t o[16];
+            tmem_ld16(tO + c * 16, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st16(tO + c * 16, o);
+          }
+        }
+      }
+      const float mb = (m == -CUDART_INF_F) ? 0.f : m;
+
+      float sum = 0.f;
+#pragma unroll
+      for (int i = 0; i < kBN / 32; ++i) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = ex2_approx(fmaf(s[i * 32 + 2 * e], cs, -mb));
+          const float p1 = ex2_approx(fmaf(s[i * 32 + 2 * e + 1], cs, -mb));
+          sum += p0 + p1;
+          pk[e] = pack2<BF16>(p0, p1);
+        }
+        tmem_st16(tS + i * 16, pk);
+      }
+      l += sum;
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bar_p[t]);
+    }
+
+    if (n > 0) {
+      mbar_wait(&bar_o[t], (n - 1) & 1, p.err, 10);
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      const bool valid = qrow < p.Nq;
+      uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
+                      2 * (static_cast<int64_t>(b) * p.o_sb + static_cast<int64_t>(h) * p.o_sh +
+                           static_cast<int64_t>(qrow) * p.o_ss);
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c) {
+        uint32_t o[16];
+        tmem_ld16(tO + c * 16, o);
+        tmem_wait_ld();
+        uint4 w0, w1;
+        w0.x = pack2<BF16>(__uint_as_float(o[0]) * inv_l, __uint_as_float(o[1]) * inv_l);
+        w0.y = pack2<BF16>(__uint_as_float(o[2]) * inv_l, __uint_as_float(o[3]) * inv_l);
+        w0.z = pack2<BF16>(__uint_as_float(o[4]) * inv_l, __uint_as_float(o[5]) * inv_l);
+        w0.w = pack2<BF16>(__uint_as_float(o[6]) * inv_l, __uint_as_float(o[7]) * inv_l);
+        w1.x = pack2<BF16>(__uint_as_float(o[8]) * inv_l, __uint_as_float(o[9]) * inv_l);
+        w1.y = pack2<BF16>(__uint_as_float(o[10]) * inv_l, __uint_as_float(o[11]) * inv_l);
+        w1.z = pack2<BF16>(__uint_as_float(o[12]) * inv_l, __uint_as_float(o[13]) * inv_l);
+        w1.w = pack2<BF16>(__uint_as_float(o[14]) * inv_l, __uint_as_float(o[15]) * inv_l);
+        if (valid) {
+          reinterpret_cast<uint4*>(orow + c * 32)[0] = w0;
+          reinterpret_cast<uint4*>(orow + c * 32)[1] = w1;
+        }
+      }
+      if (valid) {
+        // LSE = ln(sum_j exp(sm_scale q.k_j)) = ln2 * (m + log2 l)
+        p.lse[(static_cast<int64_t>(b) * p.H + h) * p.Nq + qrow] = (m + log2f(l)) * 0.69314718055994531f;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, bool BF16>
+cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  CUtensorMap tq, tk, tv;
+  if (!make_tile_map(&tq, a.q, D, a.Nq, a.H, a.B, BF16) || !make_tile_map(&tk, a.k, D, a.Nk, a.H, a.B, BF16) ||
+      !make_tile_map(&tv, a.v, D, a.Nk, a.H, a.B, BF16))
+    return cudaErrorInvalidValue;
+  FwdParams p;
+  p.B = a.B;
+  p.H = a.H;
+  p.Nq = a.Nq;
+  p.Nk = a.Nk;
+  p.n_pairs = (a.Nq + kNQT * kBM - 1) / (kNQT * kBM);
+  p.causal = a.causal;
+  p.scale_log2 = a.sm_scale * 1.4426950408889634f;
+  p.o = const_cast<void*>(a.o.ptr);
+  p.o_sb = a.o.sb;
+  p.o_sh = a.o.sh;
+  p.o_ss = a.o.ss;
+  p.lse = a.lse;
+  p.err = a.err;
+  auto kern = fwd_kernel<D, BF16>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  const long long blocks = static_cast<long long>(p.n_pairs) * a.B * a.H;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  kern<<<static_cast<unsigned>(blocks), C::THREADS, C::SMEM, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
+  switch (a.d) {
+    case 64: return a.bf16 ? launch_fwd_t<64, true>(a, stream) : launch_fwd_t<64, false>(a, stream);
+    case 80: return a.bf16 ? launch_fwd_t<80, true>(a, stream) : launch_fwd_t<80, false>(a, stream);
+    case 128: return a.bf16 ? launch_fwd_t<128, true>(a, stream) : launch_fwd_t<128, false>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace fa

@@ -1,0 +1,52 @@
+// fa_internal.h -- host-side interface between the C ABI layer (fa_api.cu)
+// and the kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fa {
+
+// One [B, H, seq, d] tensor: base pointer and element strides (d stride 1).
+struct Tensor4 {
+  const void* ptr;
+  int64_t sb, sh, ss;
+};
+
+struct FwdArgs {
+  Tensor4 q, k, v, o;
+  float* lse;  // [B, H, Nq] fp32
+  int B, H, Nq, Nk, d;
+  float sm_scale;
+  int causal;
+  bool bf16;
+  int* err;  // device error word
+};
+
+struct BwdArgs {
+  Tensor4 q, k, v, o, dout, dq, dk, dv;
+  const float* lse;  // [B, H, Nq] fp32
+  float* ws;         // workspace: D and log2-domain LSE, [B*H][Nq_pad] each
+  int B, H, Nq, Nk, d;
+  float sm_scale;
+  int causal;
+  bool bf16;
+  int* err;
+};
+
+// Rows per query / key tile of every kernel (one TMEM lane per row).
+constexpr int kTileRows = 128;
+
+inline int nq_pad(int Nq) { return (Nq + kTileRows - 1) / kTileRows * kTileRows; }
+
+// Encodes a 4-D TMA map {d, rows, H, B} with a {64, 128, 1, 1} box and the
+// 128-byte swizzle.  Returns false if the driver rejects it.
+bool make_tile_map(CUtensorMap* map, const Tensor4& t, int d, int rows, int H, int B, bool bf16);
+
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
+// phase: 0 = all three launches; 1 = D / log2-LSE preprocess; 2 = dK, dV;
+// 3 = dQ (phases 2 and 3 read what phase 1 wrote to the workspace).
+cudaError_t launch_bwd(const BwdArgs& a, int phase, cudaStream_t stream);
+
+}  // namespace fa

@@ -1,0 +1,280 @@
+"""Thin Python binding of libfa.so (argument marshalling only).
+
+Every step of the attention path runs inside the CUDA library; this module
+only turns torch tensors into pointers, strides and sizes, passes the current
+CUDA stream and converts status codes into exceptions.  There is no fallback:
+if libfa.so is missing or the tensors are not on a CUDA device, the call
+fails loudly.
+
+Entry points mirror include/fa.h:
+
+* ``fa_fwd(q, k, v, o, lse, sm_scale, causal)``
+* ``fa_bwd(q, k, v, o, do, lse, dq, dk, dv, sm_scale, causal, workspace)``
+* ``fa_bwd_workspace_bytes(B, H, Nq, Nk, d)``
+* ``fa_last_device_error()``, ``fa_status_string(code)``, ``fa_version()``
+
+Tensors are either 4-D ``[B, H, seq, d]`` or 3-D ``[seq, heads, d]`` (the
+layout of "BUG in flash attention kernel", batch 1), with the head dimension
+contiguous; other strides are passed through to the ``*_strided`` entry
+points.  ``lse`` is float32 ``[B, H, Nq]`` (``[1, H, Nq]`` for 3-D inputs).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfa.so")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_CUDA = 3
+FA_ERR_TIMEOUT = 4
+FA_ERR_WORKSPACE = 5
+
+FA_FP16 = 0
+FA_BF16 = 1
+
+FA_BWD_PREPROCESS = 1
+FA_BWD_DKDV = 2
+FA_BWD_DQ = 3
+
+EXPORTED_SYMBOLS = (
+    "fa_fwd",
+    "fa_fwd_strided",
+    "fa_bwd_workspace_bytes",
+    "fa_bwd",
+    "fa_bwd_strided",
+    "fa_bwd_phase",
+    "fa_status_string",
+    "fa_last_device_error",
+    "fa_version",
+)
+
+
+class FaError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {fa_status_string(code)} (code {code})")
+
+
+class Strides(ctypes.Structure):
+    _fields_ = [("b", ctypes.c_int64), ("h", ctypes.c_int64), ("s", ctypes.c_int64)]
+
+
+class Layout(ctypes.Structure):
+    _fields_ = [(n, Strides) for n in ("q", "k", "v", "o", "dout", "dq", "dk", "dv")]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib() -> ctypes.CDLL:
+    """Load libfa.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m tiled_attention_07_gb300.build` "
+                               "(there is no fallback implementation)")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
+        L.fa_fwd.restype = i
+        L.fa_fwd_strided.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, ctypes.POINTER(Layout), vp]
+        L.fa_fwd_strided.restype = i
+        L.fa_bwd_workspace_bytes.argtypes = [i, i, i, i, i]
+        L.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
+        L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, ctypes.c_size_t, vp]
+        L.fa_bwd.restype = i
+        L.fa_bwd_strided.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i,
+                                     ctypes.POINTER(Layout), vp, ctypes.c_size_t, vp]
+        L.fa_bwd_strided.restype = i
+        L.fa_bwd_phase.argtypes = [i, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i,
+                                   ctypes.POINTER(Layout), vp, ctypes.c_size_t, vp]
+        L.fa_bwd_phase.restype = i
+        L.fa_status_string.argtypes = [i]
+        L.fa_status_string.restype = ctypes.c_char_p
+        L.fa_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
+        L.fa_last_device_error.restype = i
+        L.fa_version.argtypes = []
+        L.fa_version.restype = ctypes.c_char_p
+        _lib = L
+        return L
+
+
+def fa_status_string(code: int) -> str:
+    return lib().fa_status_string(int(code)).decode()
+
+
+def fa_version() -> str:
+    return lib().fa_version().decode()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return FA_FP16
+    if t.dtype == torch.bfloat16:
+        return FA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype} (fp16 or bf16)")
+
+
+def _dims(t: torch.Tensor) -> Tuple[int, int, int, int]:
+    """(B, H, seq, d) of a [B, H, seq, d] or [seq, heads, d] tensor."""
+    if t.dim() == 4:
+        return tuple(t.shape)  # type: ignore[return-value]
+    if t.dim() == 3:
+        return 1, t.shape[1], t.shape[0], t.shape[2]
+    raise ValueError(f"expected a 3-D [seq, heads, d] or 4-D [B, H, seq, d] tensor, got shape {tuple(t.shape)}")
+
+
+def _strides(t: torch.Tensor) -> Strides:
+    if t.stride(-1) != 1:
+        raise ValueError("the head dimension must be contiguous (stride 1)")
+    if t.dim() == 4:
+        return Strides(t.stride(0), t.stride(1), t.stride(2))
+    # [seq, heads, d]: a single batch; its batch stride only has to be a valid
+    # multiple of 16 bytes.
+    return Strides(max(t.shape[0], 1) * t.stride(0), t.stride(1), t.stride(0))
+
+
+def _is_bhsd_contiguous(t: torch.Tensor) -> bool:
+    return t.dim() == 4 and t.is_contiguous()
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("fa_* entry points take CUDA tensors only (no CPU path)")
+
+
+def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
+           sm_scale: float, causal: bool, stream=None) -> None:
+    """O and LSE of exact attention into the caller's ``o`` and ``lse``."""
+    _check_cuda(q, k, v, o, lse)
+    B, H, Nq, d = _dims(q)
+    _, _, Nk, _ = _dims(k)
+    dt = _dtype_code(q)
+    if lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 tensor [B, H, Nq]")
+    L = lib()
+    if all(_is_bhsd_contiguous(t) for t in (q, k, v, o)):
+        rc = L.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d, float(sm_scale),
+                      int(bool(causal)), dt, _stream(stream))
+    else:
+        lay = Layout()
+        lay.q, lay.k, lay.v, lay.o = _strides(q), _strides(k), _strides(v), _strides(o)
+        rc = L.fa_fwd_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d, float(sm_scale),
+                              int(bool(causal)), dt, ctypes.byref(lay), _stream(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd")
+
+
+def fa_bwd_workspace_bytes(B: int, H: int, Nq: int, Nk: int, d: int) -> int:
+    return int(lib().fa_bwd_workspace_bytes(B, H, Nq, Nk, d))
+
+
+def fa_bwd(q, k, v, o, do, lse, dq, dk, dv, sm_scale: float, causal: bool,
+           workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """dQ, dK, dV of sum(O * dO) into the caller's ``dq``, ``dk``, ``dv``.
+
+    ``workspace`` is a CUDA byte tensor of at least ``fa_bwd_workspace_bytes``;
+    if omitted, one is allocated here with torch (the library itself never
+    allocates).
+    """
+    _check_cuda(q, k, v, o, do, lse, dq, dk, dv, workspace)
+    B, H, Nq, d = _dims(q)
+    _, _, Nk, _ = _dims(k)
+    dt = _dtype_code(q)
+    need = fa_bwd_workspace_bytes(B, H, Nq, Nk, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    L = lib()
+    ts = (q, k, v, o, do, dq, dk, dv)
+    if all(_is_bhsd_contiguous(t) for t in ts):
+        rc = L.fa_bwd(*[_ptr(t) for t in (q, k, v, o, do, lse, dq, dk, dv)], B, H, Nq, Nk, d, float(sm_scale),
+                      int(bool(causal)), dt, _ptr(workspace), ws_bytes, _stream(stream))
+    else:
+        lay = Layout()
+        lay.q, lay.k, lay.v, lay.o = _strides(q), _strides(k), _strides(v), _strides(o)
+        lay.dout, lay.dq, lay.dk, lay.dv = _strides(do), _strides(dq), _strides(dk), _strides(dv)
+        rc = L.fa_bwd_strided(*[_ptr(t) for t in (q, k, v, o, do, lse, dq, dk, dv)], B, H, Nq, Nk, d,
+                              float(sm_scale), int(bool(causal)), dt, ctypes.byref(lay), _ptr(workspace),
+                              ws_bytes, _stream(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd")
+
+
+def fa_bwd_phase(phase: int, q, k, v, o, do, lse, dq, dk, dv, sm_scale: float, causal: bool,
+                 workspace: torch.Tensor, stream=None) -> None:
+    """One of the three launches of fa_bwd (FA_BWD_PREPROCESS, FA_BWD_DKDV,
+    FA_BWD_DQ); calling the three in order with one workspace equals fa_bwd."""
+    _check_cuda(q, k, v, o, do, lse, dq, dk, dv, workspace)
+    B, H, Nq, d = _dims(q)
+    _, _, Nk, _ = _dims(k)
+    ts = (q, k, v, o, do, dq, dk, dv)
+    lay = None
+    if not all(_is_bhsd_contiguous(t) for t in ts):
+        lay = Layout()
+        lay.q, lay.k, lay.v, lay.o = _strides(q), _strides(k), _strides(v), _strides(o)
+        lay.dout, lay.dq, lay.dk, lay.dv = _strides(do), _strides(dq), _strides(dk), _strides(dv)
+    rc = lib().fa_bwd_phase(int(phase), *[_ptr(t) for t in (q, k, v, o, do, lse, dq, dk, dv)], B, H, Nq, Nk, d,
+                            float(sm_scale), int(bool(causal)), _dtype_code(q),
+                            None if lay is None else ctypes.byref(lay), _ptr(workspace),
+                            workspace.numel() * workspace.element_size(), _stream(stream))
+    if rc != FA_OK:
+        raise FaError(rc, f"fa_bwd_phase({phase})")
+
+
+def fa_last_device_error(stream=None) -> Tuple[int, int]:
+    """(status, raw device code); synchronises the stream."""
+    detail = ctypes.c_int(0)
+    rc = lib().fa_last_device_error(_stream(stream), ctypes.byref(detail))
+    return rc, detail.value
+
+
+# ---------------------------------------------------------------------------
+# conveniences that allocate the outputs with torch (plumbing, no compute)
+# ---------------------------------------------------------------------------
+
+def lse_shape(q: torch.Tensor):
+    B, H, Nq, _ = _dims(q)
+    return (B, H, Nq)
+
+
+def attention_forward(q, k, v, sm_scale: float, causal: bool, stream=None):
+    o = torch.empty_like(q)
+    lse = torch.empty(lse_shape(q), dtype=torch.float32, device=q.device)
+    fa_fwd(q, k, v, o, lse, sm_scale, causal, stream)
+    return o, lse
+
+
+def attention_backward(q, k, v, o, do, lse, sm_scale: float, causal: bool, workspace=None, stream=None):
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    fa_bwd(q, k, v, o, do, lse, dq, dk, dv, sm_scale, causal, workspace, stream)
+    return dq, dk, dv
