@@ -22,7 +22,7 @@ Definitions followed (all from "[CS336] Assignment 2: Systems", section
 * the identity rowsum(P o dP) = rowsum(O o dO) = D used by the recompute
   backward (same section, "D = rowsum(O o dO)").
 
-Readings taken where the pages are open (each is listed in the design doc):
+Readings taken where the pages are open:
 
 * ``sm_scale`` is a free parameter (the pages use both 1/sqrt(d) and 0.5).
 * causal mask is top-left aligned: key j is visible to query i iff j <= i,

@@ -1,7 +1,7 @@
 """Helpers for the CUDA-vs-oracle parity tests.
 
 Tolerances (stated for the forward by the workload definition, derived for
-the backward; see DESIGN.md "Parity"):
+the backward):
 
 * forward O: max |O_gpu - O_ref| <= 2e-3 (fp16) / 1e-2 (bf16), where each
   element may in addition be off by half an ulp of the output type at
