@@ -155,6 +155,35 @@ FA_API fa_status fa_bwd_phase(int phase, const void* q, const void* k, const voi
                        fa_dtype dtype, const fa_layout* layout,
                        void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * fa_bwd_noalloc -- fa_bwd for callers that cannot allocate device memory.
+ * The pages have no counterpart to it.  It serves callers that are handed
+ * only their input and output buffers and may not allocate on their own, for
+ * example plugins inside an inference engine that plans every buffer in
+ * advance, or code that must not call cudaMalloc while it submits work.
+ * Instead of a caller workspace it uses a fixed scratch array of
+ * FA_NOALLOC_SCRATCH_BYTES that the library keeps in every GPU that loads
+ * it, until the process exits.
+ *   Arguments: as fa_bwd (contiguous [B, H, seq, d]), without the workspace.
+ *   Limit: B*H*ceil(Nq/128)*128 <= FA_NOALLOC_SCRATCH_BYTES / 8 query rows
+ *   (2,097,152; e.g. B=4, H=32, Nq=16384).  Larger problems return
+ *   FA_ERR_WORKSPACE before anything is launched.
+ *   Allocation: none (no cudaMalloc, cudaFree or allocating library call).
+ *   Set-up: the first call on a device looks up the scratch array's device
+ *   address (cudaGetSymbolAddress) with that device current; make that first
+ *   call before any stream capture.
+ *   Sharing: every call on a device uses the same scratch array, which keeps
+ *   the previous call's contents (each call's first launch overwrites every
+ *   entry its later launches read, so nothing needs clearing).  Calls whose
+ *   work can overlap on the GPU (other streams, or host threads without
+ *   ordering between them) race on the array: serialise them.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (16u << 20)
+FA_API fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                         const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                         int B, int H, int Nq, int Nk, int d, float sm_scale, int causal,
+                         fa_dtype dtype, void* stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 FA_API const char* fa_status_string(fa_status status);
 

@@ -52,6 +52,7 @@ EXPORTED_SYMBOLS = (
     "fa_bwd",
     "fa_bwd_strided",
     "fa_bwd_phase",
+    "fa_bwd_noalloc",
     "fa_status_string",
     "fa_last_device_error",
     "fa_version",
@@ -103,6 +104,8 @@ def lib() -> ctypes.CDLL:
         L.fa_bwd_phase.argtypes = [i, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i,
                                    ctypes.POINTER(Layout), vp, ctypes.c_size_t, vp]
         L.fa_bwd_phase.restype = i
+        L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
+        L.fa_bwd_noalloc.restype = i
         L.fa_status_string.argtypes = [i]
         L.fa_status_string.restype = ctypes.c_char_p
         L.fa_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
@@ -247,6 +250,29 @@ def fa_bwd_phase(phase: int, q, k, v, o, do, lse, dq, dk, dv, sm_scale: float, c
                             workspace.numel() * workspace.element_size(), _stream(stream))
     if rc != FA_OK:
         raise FaError(rc, f"fa_bwd_phase({phase})")
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, sm_scale: float, causal: bool, stream=None) -> None:
+    """fa_bwd without a workspace, for callers that cannot allocate device
+    memory (they are given only input and output buffers, e.g. plugins of an
+    engine that plans all buffers in advance).  The library's own fixed
+    16 MiB scratch array is used instead; problems needing more than that
+    (B*H*ceil(Nq/128)*128 > 2,097,152 rows) raise FaError(FA_ERR_WORKSPACE).
+    Calls that can overlap on the GPU share that array and race: serialise
+    them.  Contiguous [B, H, seq, d] tensors only."""
+    _check_cuda(q, k, v, o, do, lse, dq, dk, dv)
+    ts = (q, k, v, o, do, dq, dk, dv)
+    if not all(_is_bhsd_contiguous(t) for t in ts):
+        raise ValueError("fa_bwd_noalloc takes contiguous [B, H, seq, d] tensors")
+    B, H, Nq, d = _dims(q)
+    _, _, Nk, _ = _dims(k)
+    rc = lib().fa_bwd_noalloc(*[_ptr(t) for t in (q, k, v, o, do, lse, dq, dk, dv)], B, H, Nq, Nk, d,
+                              float(sm_scale), int(bool(causal)), _dtype_code(q), _stream(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_bwd_noalloc")
 
 
 def fa_last_device_error(stream=None) -> Tuple[int, int]:
