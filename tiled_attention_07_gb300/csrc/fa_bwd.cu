@@ -7,8 +7,8 @@
 //   dQ = sm_scale dS K,  dK = sm_scale dS^T Q.
 // dQ accumulates along key tiles and dK/dV along query tiles, so (as on that
 // page) the work is split into two passes that each recompute P:
-//   bwd_pre_kernel   D_i and L_i * log2(e) per query row into the workspace
-//                    (padded to whole 128-row tiles: D = 0, L = +inf)
+//   bwd_pre_kernel   D_i and -L_i * log2(e) per query row into the workspace
+//                    (padded to whole 128-row tiles: D = 0, -L = -inf)
 //   dkdv_kernel      one CTA per 128-key tile, loop over query tiles:
 //                    S^T = K Q_i^T, dP^T = V dO_i^T (TMEM), P^T and dS^T by
 //                    eight elementwise warps, dV += P^T dO_i, dK += dS^T Q_i
@@ -55,7 +55,7 @@ __device__ __forceinline__ float2 unpack2(uint32_t w) {
 }
 
 // ---------------------------------------------------------------------------
-// D = rowsum(O o dO), L2 = LSE * log2(e), padded per (b, h) to Nqp rows
+// D = rowsum(O o dO), nL = -LSE * log2(e), padded per (b, h) to Nqp rows
 // ---------------------------------------------------------------------------
 struct PreParams {
   const void* o;
@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreParams p) {
   acc += __shfl_xor_sync(0xffffffffu, acc, 1);
   if (active && sub == 0) {
     p.wsD[row] = valid ? acc : 0.f;
-    p.wsL[row] = valid ? p.lse[static_cast<long long>(bh) * p.Nq + q] * kLog2e : CUDART_INF_F;
+    p.wsL[row] = valid ? -p.lse[static_cast<long long>(bh) * p.Nq + q] * kLog2e : -CUDART_INF_F;
   }
 }
 
@@ -363,8 +363,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           pt[32 + e] = __uint_as_float(r2[e]);
         }
       }
+      // P^T = exp2(c S^T - L log2 e); sL holds -L log2 e
+      const uint64_t cs2 = f2pack(cs, cs);
 #pragma unroll
-      for (int e = 0; e < 64; ++e) pt[e] = ex2_approx(fmaf(pt[e], cs, -sL[e]));
+      for (int e = 0; e < 64; e += 4) {
+        const float4 nl = *reinterpret_cast<const float4*>(sL + e);
+        float x0, x1, x2, x3;
+        f2unpack(ffma2(f2pack(pt[e], pt[e + 1]), cs2, f2pack(nl.x, nl.y)), x0, x1);
+        f2unpack(ffma2(f2pack(pt[e + 2], pt[e + 3]), cs2, f2pack(nl.z, nl.w)), x2, x3);
+        pt[e] = ex2_approx(x0);
+        pt[e + 1] = ex2_approx(x1);
+        pt[e + 2] = ex2_approx(x2);
+        pt[e + 3] = ex2_approx(x3);
+      }
       if (diag) {
 #pragma unroll
         for (int e = 0; e < 64; ++e)
@@ -389,15 +400,33 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         uint32_t r2[32];
         tmem_ld32(tdP + 32, r2);
         tmem_wait_ld();
+        // dS^T = P^T o (dP^T - D)
         uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float a0 = pt[2 * e] * (__uint_as_float(r[2 * e]) - sD[2 * e]);
-          const float a1 = pt[2 * e + 1] * (__uint_as_float(r[2 * e + 1]) - sD[2 * e + 1]);
+        for (int e = 0; e < 16; e += 2) {
+          const float4 da = *reinterpret_cast<const float4*>(sD + 2 * e);
+          const float4 db = *reinterpret_cast<const float4*>(sD + 32 + 2 * e);
+          float a0, a1, a2, a3, b0, b1, b2, b3;
+          f2unpack(fmul2(fsub2(f2pack(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])),
+                               f2pack(da.x, da.y)),
+                         f2pack(pt[2 * e], pt[2 * e + 1])),
+                   a0, a1);
+          f2unpack(fmul2(fsub2(f2pack(__uint_as_float(r[2 * e + 2]), __uint_as_float(r[2 * e + 3])),
+                               f2pack(da.z, da.w)),
+                         f2pack(pt[2 * e + 2], pt[2 * e + 3])),
+                   a2, a3);
+          f2unpack(fmul2(fsub2(f2pack(__uint_as_float(r2[2 * e]), __uint_as_float(r2[2 * e + 1])),
+                               f2pack(db.x, db.y)),
+                         f2pack(pt[32 + 2 * e], pt[32 + 2 * e + 1])),
+                   b0, b1);
+          f2unpack(fmul2(fsub2(f2pack(__uint_as_float(r2[2 * e + 2]), __uint_as_float(r2[2 * e + 3])),
+                               f2pack(db.z, db.w)),
+                         f2pack(pt[32 + 2 * e + 2], pt[32 + 2 * e + 3])),
+                   b2, b3);
           pk[e] = pack2<BF16>(a0, a1);
-          const float b0 = pt[32 + 2 * e] * (__uint_as_float(r2[2 * e]) - sD[32 + 2 * e]);
-          const float b1 = pt[32 + 2 * e + 1] * (__uint_as_float(r2[2 * e + 1]) - sD[32 + 2 * e + 1]);
+          pk[e + 1] = pack2<BF16>(a2, a3);
           pk[16 + e] = pack2<BF16>(b0, b1);
+          pk[16 + e + 1] = pack2<BF16>(b2, b3);
         }
         tmem_st16(tdP, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
         tmem_st16(tdP + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
@@ -577,8 +606,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const uint32_t tdP = tmem + lane_off + 128 + g * 64;
     const float cs = p.scale_log2;
     const int64_t wrow = static_cast<int64_t>(bh) * p.Nqp + qrow;
-    const float Lr = p.wsL[wrow];   // +inf on padded rows
+    const float nLr = p.wsL[wrow];   // -L log2 e; -inf on padded rows
     const float Dr = p.wsD[wrow];
+    const uint64_t cs2 = f2pack(cs, cs);
+    const uint64_t nl2 = f2pack(nLr, nLr);
+    const uint64_t d2 = f2pack(Dr, Dr);
 
     for (int jt = 0; jt < n_jt; ++jt) {
       const int kb = jt * kT + g * 64;   // first key of this half
@@ -603,7 +635,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       tc_fence_before();
       mbar_arrive(bar_sfree);
 #pragma unroll
-      for (int e = 0; e < 64; ++e) pr[e] = ex2_approx(fmaf(pr[e], cs, -Lr));
+      for (int e = 0; e < 64; e += 2) {
+        float x0, x1;
+        f2unpack(ffma2(f2pack(pr[e], pr[e + 1]), cs2, nl2), x0, x1);
+        pr[e] = ex2_approx(x0);
+        pr[e + 1] = ex2_approx(x1);
+      }
       if (need_mask) {
 #pragma unroll
         for (int e = 0; e < 64; ++e)
@@ -617,13 +654,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         uint32_t r2[32];
         tmem_ld32(tdP + 32, r2);
         tmem_wait_ld();
+        // dS = P o (dP - D)
         uint32_t pk[32];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          pk[e] = pack2<BF16>(pr[2 * e] * (__uint_as_float(r[2 * e]) - Dr),
-                              pr[2 * e + 1] * (__uint_as_float(r[2 * e + 1]) - Dr));
-          pk[16 + e] = pack2<BF16>(pr[32 + 2 * e] * (__uint_as_float(r2[2 * e]) - Dr),
-                                   pr[32 + 2 * e + 1] * (__uint_as_float(r2[2 * e + 1]) - Dr));
+          float a0, a1, b0, b1;
+          f2unpack(fmul2(fsub2(f2pack(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])), d2),
+                         f2pack(pr[2 * e], pr[2 * e + 1])),
+                   a0, a1);
+          f2unpack(fmul2(fsub2(f2pack(__uint_as_float(r2[2 * e]), __uint_as_float(r2[2 * e + 1])), d2),
+                         f2pack(pr[32 + 2 * e], pr[32 + 2 * e + 1])),
+                   b0, b1);
+          pk[e] = pack2<BF16>(a0, a1);
+          pk[16 + e] = pack2<BF16>(b0, b1);
         }
         tmem_st16(tdP, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
         tmem_st16(tdP + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));

@@ -75,6 +75,35 @@ __device__ __forceinline__ int key_tiles(int r0, int Nq, int Nk, int causal) {
   return n;
 }
 
+// S_t = Q_t K^T : M = 128 queries, N = 128 keys, K = D (16 per MMA), both
+// operands K-major.
+template <int D, bool BF16>
+__device__ __forceinline__ void issue_s(uint32_t tmem, uint32_t sq_addr, uint32_t skv_addr, int t, int slot) {
+  constexpr uint32_t idesc = make_idesc_f16(BF16, kBM, kBN, false, false);
+  constexpr int TILE = FwdCfg<D>::TILE;
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    const uint32_t off = (ks >> 2) * kChunkBytes + (ks & 3) * 32;
+    const uint64_t ad = make_sdesc_sw128(sq_addr + t * TILE + off, 16, 1024);
+    const uint64_t bd = make_sdesc_sw128(skv_addr + slot * TILE + off, 16, 1024);
+    umma_ss(tmem + t * 128, ad, bd, idesc, ks > 0);
+  }
+}
+
+// O_t += P_t V : M = 128 queries, N = D, K = 128 keys (16 per MMA); P_t
+// (16-bit, two per column) sits in TMEM columns [128 t, 128 t + 64), V is the
+// MN-major B operand.
+template <int D, bool BF16>
+__device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t skv_addr, int t, int slot, bool acc) {
+  constexpr uint32_t idesc = make_idesc_f16(BF16, kBM, D, false, true);
+  constexpr int TILE = FwdCfg<D>::TILE;
+#pragma unroll
+  for (int ks = 0; ks < kBN / 16; ++ks) {
+    const uint64_t bd = make_sdesc_sw128(skv_addr + slot * TILE + ks * 16 * 128, kChunkBytes, 1024);
+    umma_ts(tmem + 256 + t * 128, tmem + t * 128 + ks * 8, bd, idesc, (acc || ks > 0) ? 1u : 0u);
+  }
+}
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -173,30 +202,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   } else if (warp == C::MMA_WARP) {
     // ------------------------------------------------------------------ MMA
     if (lane == 0 && n_max > 0) {
-      constexpr uint32_t idesc_s = make_idesc_f16(BF16, kBM, kBN, false, false);
-      constexpr uint32_t idesc_o = make_idesc_f16(BF16, kBM, D, false, true);
       const uint32_t sq_addr = smem_u32(sQ);
       const uint32_t skv_addr = smem_u32(sKV);
 
-      auto issue_s = [&](int t, int slot) {
-        // S_t = Q_t K^T : M = 128 queries, N = 128 keys, K = D (16 per MMA).
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * kChunkBytes + (ks & 3) * 32;
-          const uint64_t ad = make_sdesc_sw128(sq_addr + t * C::TILE + off, 16, 1024);
-          const uint64_t bd = make_sdesc_sw128(skv_addr + slot * C::TILE + off, 16, 1024);
-          umma_ss(tmem + t * 128, ad, bd, idesc_s, ks > 0);
-        }
-      };
-      auto issue_pv = [&](int t, int slot, bool acc) {
-        // O_t += P_t V : M = 128 queries, N = D, K = 128 keys (16 per MMA);
-        // P_t (16-bit, two per column) sits in TMEM columns [128 t, 128 t + 64).
-#pragma unroll
-        for (int ks = 0; ks < kBN / 16; ++ks) {
-          const uint64_t bd = make_sdesc_sw128(skv_addr + slot * C::TILE + ks * 16 * 128, kChunkBytes, 1024);
-          umma_ts(tmem + 256 + t * 128, tmem + t * 128 + ks * 8, bd, idesc_o, (acc || ks > 0) ? 1u : 0u);
-        }
-      };
 
 #pragma unroll
       for (int t = 0; t < kNQT; ++t)
@@ -211,7 +219,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 #pragma unroll
         for (int t = 0; t < kNQT; ++t)
           if (nkt[t] > 0) {
-            issue_s(t, f % C::NSTAGE);
+            issue_s<D, BF16>(tmem, sq_addr, skv_addr, t, f % C::NSTAGE);
             umma_commit(&bar_s[t]);
           }
         umma_commit(&bar_empty[f % C::NSTAGE]);
@@ -226,7 +234,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           if (j >= nkt[t]) continue;
           mbar_wait(&bar_p[t], j & 1, p.err, 5);
           tc_fence_after();
-          issue_pv(t, fv % C::NSTAGE, j > 0);
+          issue_pv<D, BF16>(tmem, skv_addr, t, fv % C::NSTAGE, j > 0);
           umma_commit(&bar_o[t]);
           if (j + 1 < nkt[t]) {
             if (!k_ready) {
@@ -234,7 +242,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
               tc_fence_after();
               k_ready = true;
             }
-            issue_s(t, fk % C::NSTAGE);
+            issue_s<D, BF16>(tmem, sq_addr, skv_addr, t, fk % C::NSTAGE);
             umma_commit(&bar_s[t]);
           }
         }
@@ -292,9 +300,16 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         for (int c = 0; c < kBN; ++c)
           if (kbase + c >= lim) s[c] = -CUDART_INF_F;
       }
-      float mx = s[0];
+      // row max: eight independent chains of 3-input max
+      float mc[8];
 #pragma unroll
-      for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
+      for (int i = 0; i < 8; ++i) mc[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+      for (int c = 16; c < kBN; c += 16) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mc[i] = fmax3(mc[i], s[c + 2 * i], s[c + 2 * i + 1]);
+      }
+      const float mx = fmax3(fmax3(mc[0], mc[1], mc[2]), fmax3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
       const float m_tile = mx * cs;
 
       if (j == 0) {
@@ -306,33 +321,52 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           const float alpha = ex2_approx(m - m_new);
           m = m_new;
           l *= alpha;
+          const uint64_t a2 = f2pack(alpha, alpha);
 #pragma unroll
           for (int c = 0; c < D / 16; ++c) {
             uint32_t o[16];
             tmem_ld16(tO + c * 16, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            for (int e = 0; e < 16; e += 2) {
+              float lo, hi;
+              f2unpack(fmul2(f2pack(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2), lo, hi);
+              o[e] = __float_as_uint(lo);
+              o[e + 1] = __float_as_uint(hi);
+            }
             tmem_st16(tO + c * 16, o);
           }
         }
       }
       const float mb = (m == -CUDART_INF_F) ? 0.f : m;
 
-      float sum = 0.f;
+      // p = exp2(c s - m) two at a time (packed FFMA), row sum in four
+      // independent packed accumulators
+      const uint64_t cs2 = f2pack(cs, cs);
+      const uint64_t nm2 = f2pack(-mb, -mb);
+      uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
       for (int i = 0; i < kBN / 32; ++i) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2_approx(fmaf(s[i * 32 + 2 * e], cs, -mb));
-          const float p1 = ex2_approx(fmaf(s[i * 32 + 2 * e + 1], cs, -mb));
-          sum += p0 + p1;
+          const int c = i * 32 + 2 * e;
+          float x0, x1;
+          f2unpack(ffma2(f2pack(s[c], s[c + 1]), cs2, nm2), x0, x1);
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
+          acc[e & 3] = fadd2(acc[e & 3], f2pack(p0, p1));
           pk[e] = pack2<BF16>(p0, p1);
         }
         tmem_st16(tS + i * 16, pk);
       }
-      l += sum;
+      {
+        float a0, a1, b0, b1;
+        f2unpack(fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3])), a0, a1);
+        (void)b0;
+        (void)b1;
+        l += a0 + a1;
+      }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&bar_p[t]);
