@@ -196,6 +196,18 @@ FA_API const char* fa_status_string(fa_status status);
  */
 FA_API fa_status fa_last_device_error(void* stream, int* detail);
 
+/*
+ * fa_inject_device_error -- test hook for failure handling.  Writes `code`
+ * (non-zero) into the current device's error word, as if a kernel's bounded
+ * wait had given up.  Kernels launched afterwards see the word set and make
+ * every wait give up at once: they finish quickly with undefined output
+ * values (never touching memory outside their arguments), and the next
+ * fa_last_device_error() reports FA_ERR_TIMEOUT with `code` as detail and
+ * clears the word.  Nothing faults or hangs on the device.  Returns
+ * FA_ERR_INVALID_ARG for code == 0, FA_ERR_CUDA if the write fails.
+ */
+FA_API fa_status fa_inject_device_error(int code);
+
 /* Library version string, e.g. "0.1.0". */
 FA_API const char* fa_version(void);
 

@@ -121,6 +121,10 @@ def test_bwd_checks_workspace_and_args(L):
     assert bwd(L, Nk=0) == fa.FA_ERR_INVALID_ARG
 
 
+def test_inject_rejects_zero_code(L):
+    assert L.fa_inject_device_error(0) == fa.FA_ERR_INVALID_ARG
+
+
 def test_binding_refuses_cpu_tensors():
     import torch
     q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)

@@ -292,6 +292,12 @@ fa_status fa_last_device_error(void* stream, int* detail) {
   return v != 0 ? FA_ERR_TIMEOUT : FA_OK;
 }
 
+fa_status fa_inject_device_error(int code) {
+  if (code == 0) return FA_ERR_INVALID_ARG;
+  if (cudaMemcpyToSymbol(fa::g_err_word, &code, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+  return FA_OK;
+}
+
 const char* fa_version(void) { return "0.1.0"; }
 
 }  // extern "C"

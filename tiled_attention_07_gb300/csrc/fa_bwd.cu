@@ -268,10 +268,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         tma_load_4d(sK + c * kChunk, &tmK, bar_kv, c * 64, k0, h, b);
         tma_load_4d(sV + c * kChunk, &tmV, bar_kv, c * 64, k0, h, b);
       }
+      int n_issued = n_it;   // one copy in flight per slot; a give-up stops the fills
       for (int it = 0; it < n_it; ++it) {
         const int s = it % NS;
         const int use = it / NS;
-        if (use > 0) mbar_wait(&bar_empty[s], (use - 1) & 1, p.err, 21);
+        if (use > 0 && (!mbar_wait(&bar_empty[s], (use - 1) & 1, p.err, 21) ||
+                        !mbar_wait_drain(&bar_full[s], (use - 1) & 1))) {
+          n_issued = it;
+          break;
+        }
         uint8_t* st = sStage + s * C::KV_STAGE;
         const int q0 = (i_first + it) * kT;
         mbar_arrive_expect_tx(&bar_full[s], 2 * C::TILE + 1024);
@@ -283,7 +288,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         bulk_load(st + 2 * C::TILE, p.wsL + off, 512, &bar_full[s]);
         bulk_load(st + 2 * C::TILE + 512, p.wsD + off, 512, &bar_full[s]);
       }
-      for (int it = max(0, n_it - NS); it < n_it; ++it) mbar_wait_drain(&bar_full[it % NS], (it / NS) & 1);
+      for (int it = max(0, n_issued - NS); it < n_issued; ++it) mbar_wait_drain(&bar_full[it % NS], (it / NS) & 1);
       mbar_wait_drain(bar_kv, 0);
     }
   } else if (warp == C::MMA_WARP) {
@@ -544,10 +549,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         tma_load_4d(sQ + c * kChunk, &tmQ, bar_q, c * 64, q0, h, b);
         tma_load_4d(sdO + c * kChunk, &tmdO, bar_q, c * 64, q0, h, b);
       }
+      int n_issued = n_jt;   // one copy in flight per slot; a give-up stops the fills
       for (int jt = 0; jt < n_jt; ++jt) {
         const int s = jt % NS;
         const int use = jt / NS;
-        if (use > 0) mbar_wait(&bar_empty[s], (use - 1) & 1, p.err, 41);
+        if (use > 0 && (!mbar_wait(&bar_empty[s], (use - 1) & 1, p.err, 41) ||
+                        !mbar_wait_drain(&bar_full[s], (use - 1) & 1))) {
+          n_issued = jt;
+          break;
+        }
         uint8_t* st = sStage + s * C::Q_STAGE;
         mbar_arrive_expect_tx(&bar_full[s], 2 * C::TILE);
         for (int c = 0; c < C::DCH; ++c) {
@@ -555,7 +565,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           tma_load_4d(st + C::TILE + c * kChunk, &tmV, &bar_full[s], c * 64, jt * kT, h, b);
         }
       }
-      for (int jt = max(0, n_jt - NS); jt < n_jt; ++jt) mbar_wait_drain(&bar_full[jt % NS], (jt / NS) & 1);
+      for (int jt = max(0, n_issued - NS); jt < n_issued; ++jt) mbar_wait_drain(&bar_full[jt % NS], (jt / NS) & 1);
       mbar_wait_drain(bar_q, 0);
     }
   } else if (warp == C::MMA_WARP) {

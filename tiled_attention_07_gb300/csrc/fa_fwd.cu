@@ -181,11 +181,19 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           tma_load_4d(sQ + t * C::TILE + c * kChunkBytes, &tmQ, &bar_q[t], c * 64, q0 + t * kBM, h, b);
       }
       // K_0, V_0, K_1, V_1, ... : the order the MMA thread consumes them in.
-      const int nfill = 2 * n_max;
+      // A slot is refilled only after its previous fill has landed (even if
+      // a consumer that gave up released it early), so each slot has at most
+      // one copy in flight and one pending expect-tx phase.  A give-up stops
+      // the fills; only the fills actually issued are drained.
+      int nfill = 2 * n_max;
       for (int f = 0; f < nfill; ++f) {
         const int s = f % C::NSTAGE;
         const int use = f / C::NSTAGE;
-        if (use > 0) mbar_wait(&bar_empty[s], (use - 1) & 1, p.err, 1);
+        if (use > 0 && (!mbar_wait(&bar_empty[s], (use - 1) & 1, p.err, 1) ||
+                        !mbar_wait_drain(&bar_full[s], (use - 1) & 1))) {
+          nfill = f;
+          break;
+        }
         mbar_arrive_expect_tx(&bar_full[s], C::TILE);
         const int j = f >> 1;
         const CUtensorMap* map = (f & 1) ? &tmV : &tmK;

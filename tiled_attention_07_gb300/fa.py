@@ -55,6 +55,7 @@ EXPORTED_SYMBOLS = (
     "fa_bwd_noalloc",
     "fa_status_string",
     "fa_last_device_error",
+    "fa_inject_device_error",
     "fa_version",
 )
 
@@ -110,6 +111,8 @@ def lib() -> ctypes.CDLL:
         L.fa_status_string.restype = ctypes.c_char_p
         L.fa_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
         L.fa_last_device_error.restype = i
+        L.fa_inject_device_error.argtypes = [i]
+        L.fa_inject_device_error.restype = i
         L.fa_version.argtypes = []
         L.fa_version.restype = ctypes.c_char_p
         _lib = L
@@ -280,6 +283,13 @@ def fa_last_device_error(stream=None) -> Tuple[int, int]:
     detail = ctypes.c_int(0)
     rc = lib().fa_last_device_error(_stream(stream), ctypes.byref(detail))
     return rc, detail.value
+
+
+def fa_inject_device_error(code: int) -> None:
+    """Test hook: set the device error word as if a bounded wait had given up."""
+    rc = lib().fa_inject_device_error(int(code))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_inject_device_error")
 
 
 # ---------------------------------------------------------------------------
