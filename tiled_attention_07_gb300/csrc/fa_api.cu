@@ -196,12 +196,13 @@ bool make_tile_map(CUtensorMap* map, const Tensor4& t, int d, int rows, int H, i
                               static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(t.ss * 2), static_cast<cuuint64_t>(t.sh * 2),
                                  static_cast<cuuint64_t>(t.sb * 2)};
-  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(kTileRows), 1, 1};
+  const int cc = chunk_cols(d);
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(cc), static_cast<cuuint32_t>(kTileRows), 1, 1};
   const cuuint32_t estride[4] = {1, 1, 1, 1};
   CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
                    const_cast<void*>(t.ptr), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   cc == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 

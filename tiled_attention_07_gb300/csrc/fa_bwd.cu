@@ -11,7 +11,7 @@
 //                    (padded to whole 128-row tiles: D = 0, -L = -inf)
 //   dkdv_kernel      one CTA per 128-key tile, loop over query tiles:
 //                    S^T = K Q_i^T, dP^T = V dO_i^T (TMEM), P^T and dS^T by
-//                    eight elementwise warps, dV += P^T dO_i, dK += dS^T Q_i
+//                    sixteen elementwise warps, dV += P^T dO_i, dK += dS^T Q_i
 //   dq_kernel        one CTA per 128-query tile, loop over key tiles:
 //                    S = Q K_j^T, dP = dO V_j^T, dS, dQ += dS K_j
 // P is exp2(c S - L log2 e) with c = sm_scale log2(e) ("Fused Attention 2":
@@ -31,7 +31,6 @@ namespace fa {
 namespace {
 
 constexpr int kT = 128;                  // rows per query / key tile
-constexpr int kChunk = 128 * 128;        // 128 rows x 64 columns x 2 bytes
 constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ const uint8_t* row_ptr(const void* base, int64_t sb, int64_t sh, int64_t ss, int b,
@@ -124,43 +123,50 @@ __global__ void zero_rows_kernel(void* x, int64_t sb, int64_t sh, int64_t ss, in
 // ---------------------------------------------------------------------------
 template <int D>
 struct BwdCfg {
-  static constexpr int DCH = (D + 63) / 64;
-  static constexpr int TILE = DCH * kChunk;
-  static constexpr int THREADS = 320;   // 8 elementwise warps, producer, MMA
-  static constexpr int PROD_WARP = 8;
-  static constexpr int MMA_WARP = 9;
+  using G = TileGeo<D>;
+  static constexpr int TILE = G::TILE;
+  static constexpr int EW_WARPS = 16;   // 4 warpgroups x 32 columns of the 128-wide tile
+  static constexpr int THREADS = EW_WARPS * 32 + 96;   // + producer + 2 MMA issuers
+  static constexpr int PROD_WARP = EW_WARPS;
+  static constexpr int MMA_WARP = EW_WARPS + 1;   // issuer A (also allocates TMEM); issuer B follows
   // dK/dV: K, V resident; ring of (Q_i, dO_i, L_i, D_i)
-  static constexpr int KV_NSTAGE = D <= 64 ? 4 : 2;
+  static constexpr int KV_NSTAGE = D == 64 ? 5 : (D == 80 ? 3 : 2);
   static constexpr int KV_STAGE = 2 * TILE + 2 * 512;
-  static constexpr int KV_SMEM = 1024 + 2 * TILE + KV_NSTAGE * KV_STAGE + 256;
+  static constexpr int KV_SMEM = 1024 + 2 * TILE + KV_NSTAGE * KV_STAGE + 512;
   // dQ: Q, dO resident; ring of (K_j, V_j)
-  static constexpr int Q_NSTAGE = D <= 64 ? 4 : 2;
+  static constexpr int Q_NSTAGE = D == 64 ? 5 : (D == 80 ? 3 : 2);
   static constexpr int Q_STAGE = 2 * TILE;
-  static constexpr int Q_SMEM = 1024 + 2 * TILE + Q_NSTAGE * Q_STAGE + 256;
+  static constexpr int Q_SMEM = 1024 + 2 * TILE + Q_NSTAGE * Q_STAGE + 512;
 };
 
 // TMEM column of the A operand for K-step ks (16 elements) when the 16-bit
-// matrix was written by two warpgroups, each packing its 64 columns into the
-// first 32 columns of its own 64-column half.
-__device__ __forceinline__ uint32_t split_a_col(int ks) { return (ks >> 2) * 64 + (ks & 3) * 8; }
+// matrix was written by four warpgroups, each packing its 32 columns into the
+// first 16 columns of its own 32-column quarter.
+__device__ __forceinline__ uint32_t split_a_col(int ks) { return (ks >> 1) * 32 + (ks & 1) * 8; }
 
-// M = 128 x N = 128 x K = D, both operands K-major in 128B-swizzled tiles.
+// M = 128 x N = 128 x K = D, both operands K-major in swizzled tiles.
 template <int D>
 __device__ __forceinline__ void mma_nt(uint32_t d_tmem, uint32_t a_addr, uint32_t b_addr, uint32_t idesc) {
+  using G = TileGeo<D>;
 #pragma unroll
   for (int ks = 0; ks < D / 16; ++ks) {
-    const uint32_t off = (ks >> 2) * kChunk + (ks & 3) * 32;
-    umma_ss(d_tmem, make_sdesc_sw128(a_addr + off, 16, 1024), make_sdesc_sw128(b_addr + off, 16, 1024), idesc,
-            ks > 0);
+    const uint32_t off = (ks / G::KPC) * G::CHB + (ks % G::KPC) * 32;
+    umma_ss(d_tmem, make_sdesc(a_addr + off, 16, G::SBO, G::LAYOUT), make_sdesc(b_addr + off, 16, G::SBO, G::LAYOUT),
+            idesc, ks > 0);
   }
 }
 
 // D(128 x D) (+)= A(TMEM, 128 x 128) * B(128 x D, MN-major tile of 128 rows).
+// A is either split over four 32-column quarters (split_a_col) or packed
+// contiguously (8 columns per K-step).
+template <int D, bool kContiguousA = false>
 __device__ __forceinline__ void mma_tn(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_addr, uint32_t idesc,
                                        bool acc) {
+  using G = TileGeo<D>;
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
-    umma_ts(d_tmem, a_tmem + split_a_col(ks), make_sdesc_sw128(b_addr + ks * 16 * 128, kChunk, 1024), idesc,
+    const uint32_t acol = kContiguousA ? static_cast<uint32_t>(ks * 8) : split_a_col(ks);
+    umma_ts(d_tmem, a_tmem + acol, make_sdesc(b_addr + ks * 16 * G::ROWB, G::CHB, G::SBO, G::LAYOUT), idesc,
             (acc || ks > 0) ? 1u : 0u);
   }
 }
@@ -208,6 +214,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                 const MainParams p) {
   using C = BwdCfg<D>;
   constexpr int NS = C::KV_NSTAGE;
+  // With d <= 96, P^T (64 columns of packed 16-bit pairs) gets TMEM columns of
+  // its own after dV and dK, so S^T_{i+1} can be computed while the
+  // elementwise warps still work on tile i.  Otherwise it overwrites S^T.
+  constexpr bool kSepP = 256 + 2 * D + 64 <= 512;
+  constexpr uint32_t kColDV = 256;
+  constexpr uint32_t kColDK = kSepP ? 256 + D : 384;
+  constexpr uint32_t kColP = kSepP ? 256 + 2 * D : 0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = smem;
@@ -219,10 +232,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   uint64_t* bar_empty = bar_full + NS;
   uint64_t* bar_s = bar_empty + NS;   // S^T ready
   uint64_t* bar_dp = bar_s + 1;       // dP^T ready
-  uint64_t* bar_pt = bar_dp + 1;      // P^T written (256 arrivals)
-  uint64_t* bar_ds = bar_pt + 1;      // dS^T written (256 arrivals)
-  uint64_t* bar_acc = bar_ds + 1;     // all MMAs done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_acc + 1);
+  uint64_t* bar_pt = bar_dp + 1;      // P^T written (one arrival per elementwise warp)
+  uint64_t* bar_ds = bar_pt + 1;      // dS^T written
+  uint64_t* bar_acc = bar_ds + 1;     // dV, dK complete (one commit per issuer)
+  uint64_t* bar_drain = bar_acc + 1;  // every MMA of both issuers complete
+  uint64_t* bar_sfree = bar_drain + 1;  // S^T read into registers (separate-P^T layout)
+  uint64_t* bar_dvd = bar_sfree + 1;    // dV_i complete: the P^T columns are free again
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_dvd + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -241,13 +257,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     mbar_init(bar_kv, 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(&bar_full[s], 1);
-      mbar_init(&bar_empty[s], 1);
+      mbar_init(&bar_empty[s], 2);   // one release per issuer
     }
     mbar_init(bar_s, 1);
     mbar_init(bar_dp, 1);
-    mbar_init(bar_pt, 256);
-    mbar_init(bar_ds, 256);
-    mbar_init(bar_acc, 1);
+    mbar_init(bar_pt, C::EW_WARPS);   // one arrival per elementwise warp
+    mbar_init(bar_ds, C::EW_WARPS);
+    mbar_init(bar_acc, 2);
+    mbar_init(bar_drain, 2);
+    mbar_init(bar_sfree, C::EW_WARPS);
+    mbar_init(bar_dvd, 1);
     fence_mbar_init();
   }
   if (warp == C::MMA_WARP) {
@@ -264,9 +283,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmdO);
       mbar_arrive_expect_tx(bar_kv, 2 * C::TILE);
-      for (int c = 0; c < C::DCH; ++c) {
-        tma_load_4d(sK + c * kChunk, &tmK, bar_kv, c * 64, k0, h, b);
-        tma_load_4d(sV + c * kChunk, &tmV, bar_kv, c * 64, k0, h, b);
+      for (int c = 0; c < C::G::NCH; ++c) {
+        tma_load_4d(sK + c * C::G::CHB, &tmK, bar_kv, c * C::G::CC, k0, h, b);
+        tma_load_4d(sV + c * C::G::CHB, &tmV, bar_kv, c * C::G::CC, k0, h, b);
       }
       int n_issued = n_it;   // one copy in flight per slot; a give-up stops the fills
       for (int it = 0; it < n_it; ++it) {
@@ -280,9 +299,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         uint8_t* st = sStage + s * C::KV_STAGE;
         const int q0 = (i_first + it) * kT;
         mbar_arrive_expect_tx(&bar_full[s], 2 * C::TILE + 1024);
-        for (int c = 0; c < C::DCH; ++c) {
-          tma_load_4d(st + c * kChunk, &tmQ, &bar_full[s], c * 64, q0, h, b);
-          tma_load_4d(st + C::TILE + c * kChunk, &tmdO, &bar_full[s], c * 64, q0, h, b);
+        for (int c = 0; c < C::G::NCH; ++c) {
+          tma_load_4d(st + c * C::G::CHB, &tmQ, &bar_full[s], c * C::G::CC, q0, h, b);
+          tma_load_4d(st + C::TILE + c * C::G::CHB, &tmdO, &bar_full[s], c * C::G::CC, q0, h, b);
         }
         const int64_t off = static_cast<int64_t>(bh) * p.Nqp + q0;
         bulk_load(st + 2 * C::TILE, p.wsL + off, 512, &bar_full[s]);
@@ -291,87 +310,106 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       for (int it = max(0, n_issued - NS); it < n_issued; ++it) mbar_wait_drain(&bar_full[it % NS], (it / NS) & 1);
       mbar_wait_drain(bar_kv, 0);
     }
-  } else if (warp == C::MMA_WARP) {
+  } else if (warp >= C::MMA_WARP) {
+    // Two issuers: A (warp 9) computes S^T_i and dV, B (warp 10) dP^T_i and
+    // dK, so that one issuer's barrier polls are covered by the other's MMAs.
+    // Each releases every stage once (the empty barriers count two).
+    const bool issuer_a = warp == C::MMA_WARP;
     if (lane == 0 && n_it > 0) {
       constexpr uint32_t idesc_nt = make_idesc_f16(BF16, kT, kT, false, false);
       constexpr uint32_t idesc_tn = make_idesc_f16(BF16, kT, D, false, true);
       const uint32_t sk = smem_u32(sK);
       const uint32_t sv = smem_u32(sV);
       const uint32_t sst = smem_u32(sStage);
-      const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
       mbar_wait(bar_kv, 0, p.err, 22);
-      mbar_wait(&bar_full[0], 0, p.err, 23);
-      tc_fence_after();
-      mma_nt<D>(tS, sk, sst, idesc_nt);                 // S^T_0 = K Q_0^T
-      umma_commit(bar_s);
-      mma_nt<D>(tdP, sv, sst + C::TILE, idesc_nt);      // dP^T_0 = V dO_0^T
-      umma_commit(bar_dp);
       for (int it = 0; it < n_it; ++it) {
         const int s = it % NS;
         const uint32_t sq = sst + s * C::KV_STAGE;
         const uint32_t sdo = sq + C::TILE;
-        mbar_wait(bar_pt, it & 1, p.err, 24);
+        mbar_wait(&bar_full[s], (it / NS) & 1, p.err, 23);
         tc_fence_after();
-        mma_tn(tdV, tS, sdo, idesc_tn, it > 0);          // dV += P^T dO_i
-        if (it + 1 < n_it) {
-          const int s1 = (it + 1) % NS;
-          mbar_wait(&bar_full[s1], ((it + 1) / NS) & 1, p.err, 25);
-          tc_fence_after();
-          mma_nt<D>(tS, sk, sst + s1 * C::KV_STAGE, idesc_nt);   // S^T_{i+1}
-          umma_commit(bar_s);
-        }
-        mbar_wait(bar_ds, it & 1, p.err, 26);
-        tc_fence_after();
-        mma_tn(tdK, tdP, sq, idesc_tn, it > 0);          // dK += dS^T Q_i
-        umma_commit(&bar_empty[s]);
-        if (it + 1 < n_it) {
-          const int s1 = (it + 1) % NS;
-          mma_nt<D>(tdP, sv, sst + s1 * C::KV_STAGE + C::TILE, idesc_nt);   // dP^T_{i+1}
+        if (issuer_a) {
+          if (kSepP) {
+            // S^T_i was issued one step ahead (below); issue S^T_{i+1} as soon
+            // as the elementwise warps hold S^T_i in registers.
+            if (it == 0) {
+              mma_nt<D>(tmem, sk, sq, idesc_nt);          // S^T_0 = K Q_0^T
+              umma_commit(bar_s);
+            }
+            if (it + 1 < n_it) {
+              const int s1 = (it + 1) % NS;
+              mbar_wait(&bar_full[s1], ((it + 1) / NS) & 1, p.err, 25);
+              mbar_wait(bar_sfree, it & 1, p.err, 31);
+              tc_fence_after();
+              mma_nt<D>(tmem, sk, sst + s1 * C::KV_STAGE, idesc_nt);   // S^T_{i+1}
+              umma_commit(bar_s);
+            }
+            mbar_wait(bar_pt, it & 1, p.err, 24);
+            tc_fence_after();
+            mma_tn<D, true>(tmem + kColDV, tmem + kColP, sdo, idesc_tn, it > 0);  // dV += P^T_i dO_i
+            umma_commit(bar_dvd);
+          } else {
+            mma_nt<D>(tmem, sk, sq, idesc_nt);            // S^T_i = K Q_i^T
+            umma_commit(bar_s);
+            mbar_wait(bar_pt, it & 1, p.err, 24);
+            tc_fence_after();
+            mma_tn<D>(tmem + kColDV, tmem, sdo, idesc_tn, it > 0);  // dV += P^T_i dO_i
+          }
+        } else {
+          mma_nt<D>(tmem + 128, sv, sdo, idesc_nt);       // dP^T_i = V dO_i^T
           umma_commit(bar_dp);
+          mbar_wait(bar_ds, it & 1, p.err, 26);
+          tc_fence_after();
+          mma_tn<D>(tmem + kColDK, tmem + 128, sq, idesc_tn, it > 0);  // dK += dS^T_i Q_i
         }
+        umma_commit(&bar_empty[s]);
       }
       umma_commit(bar_acc);
-      mbar_wait_drain(bar_acc, 0);
+    }
+    if (lane == 0) {
+      umma_commit(bar_drain);
+      mbar_wait_drain(bar_drain, 0);
     }
   } else {
     // ------------------------------------------------------- elementwise
-    const int g = warp >> 2;             // query-column half
+    // Warpgroup g owns query columns [32 g, 32 g + 32) of S^T / dP^T; warp % 4
+    // selects the 32 key rows (TMEM lanes) of its thread.
+    const int g = warp >> 2;
     const int quad = warp & 3;
     const int krow = k0 + quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t tS = tmem + lane_off + g * 64;
-    const uint32_t tdP = tmem + lane_off + 128 + g * 64;
-    const float cs = p.scale_log2;
+    const uint32_t tS = tmem + lane_off + g * 32;
+    const uint32_t tdP = tmem + lane_off + 128 + g * 32;
+    const uint32_t tP = tmem + lane_off + kColP + g * (kSepP ? 16 : 32);
+    const uint64_t cs2 = f2pack(p.scale_log2, p.scale_log2);
 
     for (int it = 0; it < n_it; ++it) {
       const int s = it % NS;
-      const float* sL = reinterpret_cast<const float*>(sStage + s * C::KV_STAGE + 2 * C::TILE) + g * 64;
+      const float* sL = reinterpret_cast<const float*>(sStage + s * C::KV_STAGE + 2 * C::TILE) + g * 32;
       const float* sD = sL + 128;
-      const int q0 = (i_first + it) * kT + g * 64;   // first query of this half
+      const int q0 = (i_first + it) * kT + g * 32;   // first query of this quarter
       const bool diag = p.causal && (q0 < k0 + kT - 1);   // some column q < some row k
 
       mbar_wait(bar_s, it & 1, p.err, 27);
-      // L/D of this stage are in shared memory once the stage's TMA landed;
-      // S^T_i completing implies the stage was waited on by the MMA thread.
+      // L and D of this stage are in shared memory once its copy landed.
       mbar_wait(&bar_full[s], (it / NS) & 1, p.err, 28);
       tc_fence_after();
-      float pt[64];
+      float pt[32];
       {
         uint32_t r[32];
         tmem_ld32(tS, r);
-        uint32_t r2[32];
-        tmem_ld32(tS + 32, r2);
         tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          pt[e] = __uint_as_float(r[e]);
-          pt[32 + e] = __uint_as_float(r2[e]);
-        }
+        for (int e = 0; e < 32; ++e) pt[e] = __uint_as_float(r[e]);
+      }
+      if (kSepP) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_sfree);   // S^T_i is in registers
       }
       // P^T = exp2(c S^T - L log2 e); sL holds -L log2 e
-      const uint64_t cs2 = f2pack(cs, cs);
 #pragma unroll
-      for (int e = 0; e < 64; e += 4) {
+      for (int e = 0; e < 32; e += 4) {
         const float4 nl = *reinterpret_cast<const float4*>(sL + e);
         float x0, x1, x2, x3;
         f2unpack(ffma2(f2pack(pt[e], pt[e + 1]), cs2, f2pack(nl.x, nl.y)), x0, x1);
@@ -383,79 +421,71 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       }
       if (diag) {
 #pragma unroll
-        for (int e = 0; e < 64; ++e)
+        for (int e = 0; e < 32; ++e)
           if (q0 + e < krow) pt[e] = 0.f;
       }
       {
-        uint32_t pk[32];
+        uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) pk[e] = pack2<BF16>(pt[2 * e], pt[2 * e + 1]);
-        tmem_st16(tS, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-        tmem_st16(tS + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+        for (int e = 0; e < 16; ++e) pk[e] = pack2<BF16>(pt[2 * e], pt[2 * e + 1]);
+        if (kSepP && it > 0) {
+          mbar_wait(bar_dvd, (it - 1) & 1, p.err, 32);   // dV_{i-1} has read P^T_{i-1}
+          tc_fence_after();
+        }
+        tmem_st16(tP, pk);
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar_pt);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_pt);
 
       mbar_wait(bar_dp, it & 1, p.err, 29);
       tc_fence_after();
       {
         uint32_t r[32];
         tmem_ld32(tdP, r);
-        uint32_t r2[32];
-        tmem_ld32(tdP + 32, r2);
         tmem_wait_ld();
         // dS^T = P^T o (dP^T - D)
-        uint32_t pk[32];
+        uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 16; e += 2) {
-          const float4 da = *reinterpret_cast<const float4*>(sD + 2 * e);
-          const float4 db = *reinterpret_cast<const float4*>(sD + 32 + 2 * e);
-          float a0, a1, a2, a3, b0, b1, b2, b3;
-          f2unpack(fmul2(fsub2(f2pack(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])),
-                               f2pack(da.x, da.y)),
-                         f2pack(pt[2 * e], pt[2 * e + 1])),
+        for (int e = 0; e < 32; e += 4) {
+          const float4 dd = *reinterpret_cast<const float4*>(sD + e);
+          float a0, a1, a2, a3;
+          f2unpack(fmul2(fsub2(f2pack(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), f2pack(dd.x, dd.y)),
+                         f2pack(pt[e], pt[e + 1])),
                    a0, a1);
-          f2unpack(fmul2(fsub2(f2pack(__uint_as_float(r[2 * e + 2]), __uint_as_float(r[2 * e + 3])),
-                               f2pack(da.z, da.w)),
-                         f2pack(pt[2 * e + 2], pt[2 * e + 3])),
+          f2unpack(fmul2(fsub2(f2pack(__uint_as_float(r[e + 2]), __uint_as_float(r[e + 3])), f2pack(dd.z, dd.w)),
+                         f2pack(pt[e + 2], pt[e + 3])),
                    a2, a3);
-          f2unpack(fmul2(fsub2(f2pack(__uint_as_float(r2[2 * e]), __uint_as_float(r2[2 * e + 1])),
-                               f2pack(db.x, db.y)),
-                         f2pack(pt[32 + 2 * e], pt[32 + 2 * e + 1])),
-                   b0, b1);
-          f2unpack(fmul2(fsub2(f2pack(__uint_as_float(r2[2 * e + 2]), __uint_as_float(r2[2 * e + 3])),
-                               f2pack(db.z, db.w)),
-                         f2pack(pt[32 + 2 * e + 2], pt[32 + 2 * e + 3])),
-                   b2, b3);
-          pk[e] = pack2<BF16>(a0, a1);
-          pk[e + 1] = pack2<BF16>(a2, a3);
-          pk[16 + e] = pack2<BF16>(b0, b1);
-          pk[16 + e + 1] = pack2<BF16>(b2, b3);
+          pk[e / 2] = pack2<BF16>(a0, a1);
+          pk[e / 2 + 1] = pack2<BF16>(a2, a3);
         }
-        tmem_st16(tdP, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-        tmem_st16(tdP + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+        tmem_st16(tdP, pk);
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar_ds);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_ds);
     }
 
-    // epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK * sm_scale
+    // epilogue: warpgroups 0-1 write dV, 2-3 write dK * sm_scale (16-column
+    // chunks alternate between the two warpgroups of each)
     if (n_it > 0) {
       mbar_wait(bar_acc, 0, p.err, 30);
       tc_fence_after();
     }
+    const bool is_dk = g >= 2;
     const bool valid = krow < p.Nk;
-    void* outp = g == 0 ? p.out0 : p.out1;
-    const int64_t sb = g == 0 ? p.o0_sb : p.o1_sb;
-    const int64_t sh = g == 0 ? p.o0_sh : p.o1_sh;
-    const int64_t ss = g == 0 ? p.o0_ss : p.o1_ss;
-    const float scale = g == 0 ? 1.f : p.sm_scale;
+    void* outp = is_dk ? p.out1 : p.out0;
+    const int64_t sb = is_dk ? p.o1_sb : p.o0_sb;
+    const int64_t sh = is_dk ? p.o1_sh : p.o0_sh;
+    const int64_t ss = is_dk ? p.o1_ss : p.o0_ss;
+    const float scale = is_dk ? p.sm_scale : 1.f;
     uint8_t* dst = const_cast<uint8_t*>(row_ptr(outp, sb, sh, ss, b, h, krow));
-    const uint32_t tacc = tmem + lane_off + (g == 0 ? 256 : 384);
+    const uint32_t tacc = tmem + lane_off + (is_dk ? kColDK : kColDV);
 #pragma unroll
     for (int c = 0; c < D / 16; ++c) {
+      if ((c & 1) != (g & 1)) continue;
       uint32_t v[16];
       if (n_it > 0) {
         tmem_ld16(tacc + c * 16, v);
@@ -480,7 +510,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 // dQ: one CTA per (query tile, b, h)
 // ---------------------------------------------------------------------------
 // TMEM columns: [0,128) S, [128,256) dP -> dS, [256,256+D) dQ.  Elementwise
-// warps: warpgroup g owns key columns [64 g, 64 g + 64); warp % 4 selects
+// warps: warpgroup g owns key columns [32 g, 32 g + 32); warp % 4 selects
 // the 32 query rows.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
@@ -500,10 +530,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   uint64_t* bar_empty = bar_full + NS;
   uint64_t* bar_s = bar_empty + NS;
   uint64_t* bar_dp = bar_s + 1;
-  uint64_t* bar_sfree = bar_dp + 1;   // S read into registers (256 arrivals)
-  uint64_t* bar_ds = bar_sfree + 1;   // dS written (256 arrivals)
-  uint64_t* bar_acc = bar_ds + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_acc + 1);
+  uint64_t* bar_sfree = bar_dp + 1;   // S read into registers (one arrival per elementwise warp)
+  uint64_t* bar_ds = bar_sfree + 1;   // dS written
+  uint64_t* bar_acc = bar_ds + 1;     // dQ complete (one commit per issuer)
+  uint64_t* bar_drain = bar_acc + 1;  // every MMA of both issuers complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_drain + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -522,13 +553,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     mbar_init(bar_q, 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(&bar_full[s], 1);
-      mbar_init(&bar_empty[s], 1);
+      mbar_init(&bar_empty[s], 2);   // one release per issuer
     }
     mbar_init(bar_s, 1);
     mbar_init(bar_dp, 1);
-    mbar_init(bar_sfree, 256);
-    mbar_init(bar_ds, 256);
-    mbar_init(bar_acc, 1);
+    mbar_init(bar_sfree, C::EW_WARPS);
+    mbar_init(bar_ds, C::EW_WARPS);
+    mbar_init(bar_acc, 2);
+    mbar_init(bar_drain, 2);
     fence_mbar_init();
   }
   if (warp == C::MMA_WARP) {
@@ -545,9 +577,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       mbar_arrive_expect_tx(bar_q, 2 * C::TILE);
-      for (int c = 0; c < C::DCH; ++c) {
-        tma_load_4d(sQ + c * kChunk, &tmQ, bar_q, c * 64, q0, h, b);
-        tma_load_4d(sdO + c * kChunk, &tmdO, bar_q, c * 64, q0, h, b);
+      for (int c = 0; c < C::G::NCH; ++c) {
+        tma_load_4d(sQ + c * C::G::CHB, &tmQ, bar_q, c * C::G::CC, q0, h, b);
+        tma_load_4d(sdO + c * C::G::CHB, &tmdO, bar_q, c * C::G::CC, q0, h, b);
       }
       int n_issued = n_jt;   // one copy in flight per slot; a give-up stops the fills
       for (int jt = 0; jt < n_jt; ++jt) {
@@ -560,92 +592,86 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         }
         uint8_t* st = sStage + s * C::Q_STAGE;
         mbar_arrive_expect_tx(&bar_full[s], 2 * C::TILE);
-        for (int c = 0; c < C::DCH; ++c) {
-          tma_load_4d(st + c * kChunk, &tmK, &bar_full[s], c * 64, jt * kT, h, b);
-          tma_load_4d(st + C::TILE + c * kChunk, &tmV, &bar_full[s], c * 64, jt * kT, h, b);
+        for (int c = 0; c < C::G::NCH; ++c) {
+          tma_load_4d(st + c * C::G::CHB, &tmK, &bar_full[s], c * C::G::CC, jt * kT, h, b);
+          tma_load_4d(st + C::TILE + c * C::G::CHB, &tmV, &bar_full[s], c * C::G::CC, jt * kT, h, b);
         }
       }
       for (int jt = max(0, n_issued - NS); jt < n_issued; ++jt) mbar_wait_drain(&bar_full[jt % NS], (jt / NS) & 1);
       mbar_wait_drain(bar_q, 0);
     }
-  } else if (warp == C::MMA_WARP) {
+  } else if (warp >= C::MMA_WARP) {
+    // Two issuers: A (warp 9) computes S_j, B (warp 10) dP_j and dQ; each
+    // releases every stage once (the empty barriers count two).
+    const bool issuer_a = warp == C::MMA_WARP;
     if (lane == 0 && n_jt > 0) {
       constexpr uint32_t idesc_nt = make_idesc_f16(BF16, kT, kT, false, false);
       constexpr uint32_t idesc_tn = make_idesc_f16(BF16, kT, D, false, true);
       const uint32_t sq = smem_u32(sQ);
       const uint32_t sdo = smem_u32(sdO);
       const uint32_t sst = smem_u32(sStage);
-      const uint32_t tS = tmem, tdP = tmem + 128, tdQ = tmem + 256;
       mbar_wait(bar_q, 0, p.err, 42);
-      mbar_wait(&bar_full[0], 0, p.err, 43);
-      tc_fence_after();
-      mma_nt<D>(tS, sq, sst, idesc_nt);                   // S_0 = Q K_0^T
-      umma_commit(bar_s);
-      mma_nt<D>(tdP, sdo, sst + C::TILE, idesc_nt);       // dP_0 = dO V_0^T
-      umma_commit(bar_dp);
       for (int jt = 0; jt < n_jt; ++jt) {
         const int s = jt % NS;
         const uint32_t sk = sst + s * C::Q_STAGE;
-        if (jt + 1 < n_jt) {
-          const int s1 = (jt + 1) % NS;
-          mbar_wait(&bar_full[s1], ((jt + 1) / NS) & 1, p.err, 44);
-          mbar_wait(bar_sfree, jt & 1, p.err, 45);
+        mbar_wait(&bar_full[s], (jt / NS) & 1, p.err, 43);
+        if (issuer_a) {
+          if (jt > 0) mbar_wait(bar_sfree, (jt - 1) & 1, p.err, 45);   // S_{j-1} read
           tc_fence_after();
-          mma_nt<D>(tS, sq, sst + s1 * C::Q_STAGE, idesc_nt);   // S_{j+1}
+          mma_nt<D>(tmem, sq, sk, idesc_nt);                // S_j = Q K_j^T
           umma_commit(bar_s);
-        }
-        mbar_wait(bar_ds, jt & 1, p.err, 46);
-        tc_fence_after();
-        mma_tn(tdQ, tdP, sk, idesc_tn, jt > 0);           // dQ += dS K_j
-        umma_commit(&bar_empty[s]);
-        if (jt + 1 < n_jt) {
-          const int s1 = (jt + 1) % NS;
-          mma_nt<D>(tdP, sdo, sst + s1 * C::Q_STAGE + C::TILE, idesc_nt);   // dP_{j+1}
+        } else {
+          tc_fence_after();
+          mma_nt<D>(tmem + 128, sdo, sk + C::TILE, idesc_nt);   // dP_j = dO V_j^T
           umma_commit(bar_dp);
+          mbar_wait(bar_ds, jt & 1, p.err, 46);
+          tc_fence_after();
+          mma_tn<D>(tmem + 256, tmem + 128, sk, idesc_tn, jt > 0);  // dQ += dS_j K_j
         }
+        umma_commit(&bar_empty[s]);
       }
       umma_commit(bar_acc);
-      mbar_wait_drain(bar_acc, 0);
+    }
+    if (lane == 0) {
+      umma_commit(bar_drain);
+      mbar_wait_drain(bar_drain, 0);
     }
   } else {
+    // Warpgroup g owns key columns [32 g, 32 g + 32) of S / dP; warp % 4
+    // selects the 32 query rows (TMEM lanes) of its thread.
     const int g = warp >> 2;
     const int quad = warp & 3;
     const int qrow = q0 + quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t tS = tmem + lane_off + g * 64;
-    const uint32_t tdP = tmem + lane_off + 128 + g * 64;
-    const float cs = p.scale_log2;
+    const uint32_t tS = tmem + lane_off + g * 32;
+    const uint32_t tdP = tmem + lane_off + 128 + g * 32;
     const int64_t wrow = static_cast<int64_t>(bh) * p.Nqp + qrow;
     const float nLr = p.wsL[wrow];   // -L log2 e; -inf on padded rows
     const float Dr = p.wsD[wrow];
-    const uint64_t cs2 = f2pack(cs, cs);
+    const uint64_t cs2 = f2pack(p.scale_log2, p.scale_log2);
     const uint64_t nl2 = f2pack(nLr, nLr);
     const uint64_t d2 = f2pack(Dr, Dr);
+    const int lim = p.causal ? min(p.Nk, qrow + 1) : p.Nk;   // keys < lim are visible
 
     for (int jt = 0; jt < n_jt; ++jt) {
-      const int kb = jt * kT + g * 64;   // first key of this half
-      const bool need_mask = (kb + 64 > p.Nk) || (p.causal && kb + 63 > q0);
-      const int lim = p.causal ? min(p.Nk, qrow + 1) : p.Nk;
+      const int kb = jt * kT + g * 32;   // first key of this quarter
+      const bool need_mask = (kb + 32 > p.Nk) || (p.causal && kb + 31 > q0);
 
       mbar_wait(bar_s, jt & 1, p.err, 47);
       tc_fence_after();
-      float pr[64];
+      float pr[32];
       {
         uint32_t r[32];
         tmem_ld32(tS, r);
-        uint32_t r2[32];
-        tmem_ld32(tS + 32, r2);
         tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          pr[e] = __uint_as_float(r[e]);
-          pr[32 + e] = __uint_as_float(r2[e]);
-        }
+        for (int e = 0; e < 32; ++e) pr[e] = __uint_as_float(r[e]);
       }
       tc_fence_before();
-      mbar_arrive(bar_sfree);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_sfree);
 #pragma unroll
-      for (int e = 0; e < 64; e += 2) {
+      for (int e = 0; e < 32; e += 2) {
         float x0, x1;
         f2unpack(ffma2(f2pack(pr[e], pr[e + 1]), cs2, nl2), x0, x1);
         pr[e] = ex2_approx(x0);
@@ -653,7 +679,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       }
       if (need_mask) {
 #pragma unroll
-        for (int e = 0; e < 64; ++e)
+        for (int e = 0; e < 32; ++e)
           if (kb + e >= lim) pr[e] = 0.f;
       }
       mbar_wait(bar_dp, jt & 1, p.err, 48);
@@ -661,32 +687,26 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       {
         uint32_t r[32];
         tmem_ld32(tdP, r);
-        uint32_t r2[32];
-        tmem_ld32(tdP + 32, r2);
         tmem_wait_ld();
         // dS = P o (dP - D)
-        uint32_t pk[32];
+        uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          float a0, a1, b0, b1;
+          float a0, a1;
           f2unpack(fmul2(fsub2(f2pack(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1])), d2),
                          f2pack(pr[2 * e], pr[2 * e + 1])),
                    a0, a1);
-          f2unpack(fmul2(fsub2(f2pack(__uint_as_float(r2[2 * e]), __uint_as_float(r2[2 * e + 1])), d2),
-                         f2pack(pr[32 + 2 * e], pr[32 + 2 * e + 1])),
-                   b0, b1);
           pk[e] = pack2<BF16>(a0, a1);
-          pk[16 + e] = pack2<BF16>(b0, b1);
         }
-        tmem_st16(tdP, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-        tmem_st16(tdP + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+        tmem_st16(tdP, pk);
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar_ds);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_ds);
     }
 
-    // epilogue: dQ * sm_scale; 16-column chunks alternate between warpgroups
+    // epilogue: dQ * sm_scale; 16-column chunk c is written by warpgroup c % 4
     if (n_jt > 0) {
       mbar_wait(bar_acc, 0, p.err, 49);
       tc_fence_after();
@@ -696,7 +716,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const uint32_t tacc = tmem + lane_off + 256;
 #pragma unroll
     for (int c = 0; c < D / 16; ++c) {
-      if ((c & 1) != g) continue;
+      if ((c & 3) != g) continue;
       uint32_t v[16];
       if (n_jt > 0) {
         tmem_ld16(tacc + c * 16, v);

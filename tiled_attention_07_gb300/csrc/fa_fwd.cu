@@ -14,12 +14,16 @@
 //   warps 4-7  the same for query tile 1
 //   warp  8    TMA producer: Q tiles once, then K_j, V_j through an
 //              mbarrier ring of NSTAGE shared-memory slots
-//   warp  9    TMEM allocator and single-thread tcgen05.mma issuer
+//   warps 9-10 tcgen05.mma issuers, one thread per query tile (warp 9 also
+//              allocates TMEM).  Two issuing threads keep the tensor pipe fed:
+//              the issue of tcgen05.mma runs at most about one MMA ahead of its
+//              execution, so every barrier poll by an issuer leaves a bubble
+//              that only the other issuer's MMAs can fill.
 // Tensor memory (512 columns x 128 lanes): S_t at column 128*t (fp32 scores,
 // overwritten in place by the 16-bit P_t that feeds the PV MMA as its A
-// operand), O_t at column 256 + 128*t (fp32 accumulator).  The MMA thread
-// ping-pongs the two tiles: while tile 0's softmax runs on S_0 the tensor
-// cores compute PV and the next S of tile 1, and the other way round.
+// operand), O_t at column 256 + 128*t (fp32 accumulator).  While tile 0's
+// softmax runs on S_0 the tensor cores compute PV and the next S of tile 1,
+// and the other way round.
 // O is rescaled in TMEM only when a row's running max grows by more than
 // 2^8 (the stale max stays exact because l uses the same max).
 // Causal: tiles above the diagonal are never loaded or computed; only the
@@ -37,20 +41,19 @@ namespace {
 constexpr int kBM = 128;          // query rows per tile
 constexpr int kBN = 128;          // keys per tile
 constexpr int kNQT = 2;           // query tiles per CTA
-constexpr int kChunkBytes = 128 * 128;  // 128 rows x 64 columns x 2 bytes
 constexpr float kRescaleLog2 = 8.0f;
 
 template <int D>
 struct FwdCfg {
-  static constexpr int DCH = (D + 63) / 64;            // 64-column chunks per row
-  static constexpr int TILE = DCH * kChunkBytes;        // one 128-row tile
-  static constexpr int NSTAGE = D <= 64 ? 8 : 4;        // K/V ring depth
+  using G = TileGeo<D>;
+  static constexpr int TILE = G::TILE;                  // one 128-row tile of Q, K or V
+  static constexpr int NSTAGE = D == 64 ? 8 : (D == 80 ? 6 : 4);   // K/V ring depth
   static constexpr int SMEM_DATA = kNQT * TILE + NSTAGE * TILE;
-  static constexpr int NBARS = kNQT + 2 * NSTAGE + 3 * kNQT + 1;
+  static constexpr int NBARS = kNQT + 2 * NSTAGE + 4 * kNQT + 1;
   static constexpr int SMEM = 1024 + SMEM_DATA + NBARS * 8 + 16;
-  static constexpr int THREADS = kNQT * 128 + 64;
+  static constexpr int THREADS = kNQT * 128 + 32 + kNQT * 32;
   static constexpr int PROD_WARP = kNQT * 4;
-  static constexpr int MMA_WARP = kNQT * 4 + 1;
+  static constexpr int MMA_WARP = kNQT * 4 + 1;   // first of kNQT issuer warps (also allocates TMEM)
 };
 
 struct FwdParams {
@@ -79,13 +82,14 @@ __device__ __forceinline__ int key_tiles(int r0, int Nq, int Nk, int causal) {
 // operands K-major.
 template <int D, bool BF16>
 __device__ __forceinline__ void issue_s(uint32_t tmem, uint32_t sq_addr, uint32_t skv_addr, int t, int slot) {
+  using G = TileGeo<D>;
   constexpr uint32_t idesc = make_idesc_f16(BF16, kBM, kBN, false, false);
   constexpr int TILE = FwdCfg<D>::TILE;
 #pragma unroll
   for (int ks = 0; ks < D / 16; ++ks) {
-    const uint32_t off = (ks >> 2) * kChunkBytes + (ks & 3) * 32;
-    const uint64_t ad = make_sdesc_sw128(sq_addr + t * TILE + off, 16, 1024);
-    const uint64_t bd = make_sdesc_sw128(skv_addr + slot * TILE + off, 16, 1024);
+    const uint32_t off = (ks / G::KPC) * G::CHB + (ks % G::KPC) * 32;
+    const uint64_t ad = make_sdesc(sq_addr + t * TILE + off, 16, G::SBO, G::LAYOUT);
+    const uint64_t bd = make_sdesc(skv_addr + slot * TILE + off, 16, G::SBO, G::LAYOUT);
     umma_ss(tmem + t * 128, ad, bd, idesc, ks > 0);
   }
 }
@@ -95,11 +99,12 @@ __device__ __forceinline__ void issue_s(uint32_t tmem, uint32_t sq_addr, uint32_
 // MN-major B operand.
 template <int D, bool BF16>
 __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t skv_addr, int t, int slot, bool acc) {
+  using G = TileGeo<D>;
   constexpr uint32_t idesc = make_idesc_f16(BF16, kBM, D, false, true);
   constexpr int TILE = FwdCfg<D>::TILE;
 #pragma unroll
   for (int ks = 0; ks < kBN / 16; ++ks) {
-    const uint64_t bd = make_sdesc_sw128(skv_addr + slot * TILE + ks * 16 * 128, kChunkBytes, 1024);
+    const uint64_t bd = make_sdesc(skv_addr + slot * TILE + ks * 16 * G::ROWB, G::CHB, G::SBO, G::LAYOUT);
     umma_ts(tmem + 256 + t * 128, tmem + t * 128 + ks * 8, bd, idesc, (acc || ks > 0) ? 1u : 0u);
   }
 }
@@ -120,7 +125,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   uint64_t* bar_s = bar_empty + C::NSTAGE;          // [kNQT] S_t ready
   uint64_t* bar_p = bar_s + kNQT;                   // [kNQT] P_t written (128 arrivals)
   uint64_t* bar_o = bar_p + kNQT;                   // [kNQT] PV_t complete
-  uint64_t* bar_drain = bar_o + kNQT;               // [1]
+  uint64_t* bar_turn = bar_o + kNQT;                // [kNQT] issuer t may issue its next group
+  uint64_t* bar_drain = bar_turn + kNQT;            // [1]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_drain + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -150,12 +156,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       mbar_init(&bar_s[t], 1);
       mbar_init(&bar_p[t], 128);
       mbar_init(&bar_o[t], 1);
+      mbar_init(&bar_turn[t], 1);
     }
     for (int s = 0; s < C::NSTAGE; ++s) {
       mbar_init(&bar_full[s], 1);
-      mbar_init(&bar_empty[s], 1);
+      mbar_init(&bar_empty[s], kNQT);   // one release per issuer
     }
-    mbar_init(bar_drain, 1);
+    mbar_init(bar_drain, kNQT);
     fence_mbar_init();
   }
   if (warp == C::MMA_WARP) {
@@ -177,8 +184,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       for (int t = 0; t < kNQT; ++t) {
         if (nkt[t] == 0) continue;
         mbar_arrive_expect_tx(&bar_q[t], C::TILE);
-        for (int c = 0; c < C::DCH; ++c)
-          tma_load_4d(sQ + t * C::TILE + c * kChunkBytes, &tmQ, &bar_q[t], c * 64, q0 + t * kBM, h, b);
+        for (int c = 0; c < C::G::NCH; ++c)
+          tma_load_4d(sQ + t * C::TILE + c * C::G::CHB, &tmQ, &bar_q[t], c * C::G::CC, q0 + t * kBM, h, b);
       }
       // K_0, V_0, K_1, V_1, ... : the order the MMA thread consumes them in.
       // A slot is refilled only after its previous fill has landed (even if
@@ -197,8 +204,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         mbar_arrive_expect_tx(&bar_full[s], C::TILE);
         const int j = f >> 1;
         const CUtensorMap* map = (f & 1) ? &tmV : &tmK;
-        for (int c = 0; c < C::DCH; ++c)
-          tma_load_4d(sKV + s * C::TILE + c * kChunkBytes, map, &bar_full[s], c * 64, j * kBN, h, b);
+        for (int c = 0; c < C::G::NCH; ++c)
+          tma_load_4d(sKV + s * C::TILE + c * C::G::CHB, map, &bar_full[s], c * C::G::CC, j * kBN, h, b);
       }
       // Drain: the last fill of every slot has landed before the CTA exits.
       for (int f = max(0, nfill - C::NSTAGE); f < nfill; ++f)
@@ -207,64 +214,55 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       for (int t = 0; t < kNQT; ++t)
         if (nkt[t] > 0) mbar_wait_drain(&bar_q[t], 0);
     }
-  } else if (warp == C::MMA_WARP) {
-    // ------------------------------------------------------------------ MMA
+  } else if (warp >= C::MMA_WARP) {
+    // ------------------------------------------------------------ MMA issue
+    // Issuer t drives query tile t.  Its groups are G(t,-1) = S_t,0 and
+    // G(t,j) = PV_t,j + S_t,j+1; the two issuers take turns in the order
+    // G(0,-1) G(1,-1) G(0,0) G(1,0) G(0,1) ..., handing over through
+    // bar_turn, which keeps the two tiles half a step apart (one tile's
+    // softmax runs while the tensor cores work for the other).  An issuer
+    // does its barrier polls for the next group before it waits for its
+    // turn, i.e. while the other issuer's MMAs execute.
+    // Every K/V fill is released by one commit of each issuer, also fills
+    // its own tile does not need, and only after the fill has landed, so
+    // both releases of one use of a slot come before any release of its next
+    // use (the empty barriers count two).
+    const int t = warp - C::MMA_WARP;
     if (lane == 0 && n_max > 0) {
       const uint32_t sq_addr = smem_u32(sQ);
       const uint32_t skv_addr = smem_u32(sKV);
-
-
-#pragma unroll
-      for (int t = 0; t < kNQT; ++t)
-        if (nkt[t] > 0) mbar_wait(&bar_q[t], 0, p.err, 2);
-      tc_fence_after();
-
-      // Prologue: S_t,0 for every tile.
-      {
-        const int f = 0;
-        mbar_wait(&bar_full[f % C::NSTAGE], (f / C::NSTAGE) & 1, p.err, 3);
+      const int nt = nkt[t];
+      // G(t,-1)
+      if (nt > 0) mbar_wait(&bar_q[t], 0, p.err, 2);
+      mbar_wait(&bar_full[0], 0, p.err, 3);
+      if (t == 1) mbar_wait(&bar_turn[1], 0, p.err, 11);
+      if (nt > 0) {
         tc_fence_after();
-#pragma unroll
-        for (int t = 0; t < kNQT; ++t)
-          if (nkt[t] > 0) {
-            issue_s<D, BF16>(tmem, sq_addr, skv_addr, t, f % C::NSTAGE);
-            umma_commit(&bar_s[t]);
-          }
-        umma_commit(&bar_empty[f % C::NSTAGE]);
+        issue_s<D, BF16>(tmem, sq_addr, skv_addr, t, 0);
       }
+      mbar_arrive(&bar_turn[1 - t]);
+      if (nt > 0) umma_commit(&bar_s[t]);
+      umma_commit(&bar_empty[0]);
       for (int j = 0; j < n_max; ++j) {
         const int fv = 2 * j + 1;            // fill index of V_j
         const int fk = 2 * j + 2;            // fill index of K_{j+1}
+        const bool pv = j < nt;
+        const bool sn = j + 1 < nt;
         mbar_wait(&bar_full[fv % C::NSTAGE], (fv / C::NSTAGE) & 1, p.err, 4);
-        bool k_ready = false;
-#pragma unroll
-        for (int t = 0; t < kNQT; ++t) {
-          if (j >= nkt[t]) continue;
-          mbar_wait(&bar_p[t], j & 1, p.err, 5);
-          tc_fence_after();
-          issue_pv<D, BF16>(tmem, skv_addr, t, fv % C::NSTAGE, j > 0);
-          umma_commit(&bar_o[t]);
-          if (j + 1 < nkt[t]) {
-            if (!k_ready) {
-              mbar_wait(&bar_full[fk % C::NSTAGE], (fk / C::NSTAGE) & 1, p.err, 6);
-              tc_fence_after();
-              k_ready = true;
-            }
-            issue_s<D, BF16>(tmem, sq_addr, skv_addr, t, fk % C::NSTAGE);
-            umma_commit(&bar_s[t]);
-          }
-        }
+        if (j + 1 < n_max) mbar_wait(&bar_full[fk % C::NSTAGE], (fk / C::NSTAGE) & 1, p.err, 6);
+        if (pv) mbar_wait(&bar_p[t], j & 1, p.err, 5);
+        // turn: G(0,j) follows G(1,j-1), G(1,j) follows G(0,j)
+        mbar_wait(&bar_turn[t], (t == 0 ? j : j + 1) & 1, p.err, 12);
+        tc_fence_after();
+        if (pv) issue_pv<D, BF16>(tmem, skv_addr, t, fv % C::NSTAGE, j > 0);
+        if (sn) issue_s<D, BF16>(tmem, sq_addr, skv_addr, t, fk % C::NSTAGE);
+        mbar_arrive(&bar_turn[1 - t]);
+        if (pv && !sn) umma_commit(&bar_o[t]);   // last PV of this tile
+        if (sn) umma_commit(&bar_s[t]);
         umma_commit(&bar_empty[fv % C::NSTAGE]);
-        if (j + 1 < n_max) {
-          if (!k_ready) {
-            // No tile uses K_{j+1}; only possible when tiles end early. Keep
-            // the ring in step with the producer.
-            mbar_wait(&bar_full[fk % C::NSTAGE], (fk / C::NSTAGE) & 1, p.err, 7);
-          }
-          umma_commit(&bar_empty[fk % C::NSTAGE]);
-        }
+        if (j + 1 < n_max) umma_commit(&bar_empty[fk % C::NSTAGE]);
       }
-      // Drain: every MMA has completed before TMEM is released.
+      // Drain: every MMA of both issuers has completed before TMEM is freed.
       umma_commit(bar_drain);
       mbar_wait_drain(bar_drain, 0);
     }
@@ -285,8 +283,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     float l = 0.f;            // running sum of exp2(score - m)
 
     for (int j = 0; j < n; ++j) {
+      // S_t,j complete implies PV_t,j-1 complete (one issuer, and a commit
+      // tracks every earlier MMA of its thread), so O_t may be rescaled.
       mbar_wait(&bar_s[t], j & 1, p.err, 8);
-      if (j > 0) mbar_wait(&bar_o[t], (j - 1) & 1, p.err, 9);
       tc_fence_after();
 
       float s[kBN];
@@ -381,7 +380,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     }
 
     if (n > 0) {
-      mbar_wait(&bar_o[t], (n - 1) & 1, p.err, 10);
+      mbar_wait(&bar_o[t], 0, p.err, 10);   // committed once, after the last PV
       tc_fence_after();
       const float inv_l = 1.f / l;
       const bool valid = qrow < p.Nq;

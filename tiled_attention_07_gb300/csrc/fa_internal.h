@@ -40,8 +40,28 @@ constexpr int kTileRows = 128;
 
 inline int nq_pad(int Nq) { return (Nq + kTileRows - 1) / kTileRows * kTileRows; }
 
-// Encodes a 4-D TMA map {d, rows, H, B} with a {64, 128, 1, 1} box and the
-// 128-byte swizzle.  Returns false if the driver rejects it.
+// Columns per swizzle chunk of a 128-row shared-memory tile: 64 (128-byte
+// rows, 128-byte swizzle) when d is a multiple of 64, else 32 (64-byte rows,
+// 64-byte swizzle), so that d = 80 pads to 96 columns instead of 128.
+__host__ __device__ constexpr int chunk_cols(int d) { return d % 64 == 0 ? 64 : 32; }
+
+// Shared-memory geometry of one 128-row tile of a [.., d] tensor as TMA
+// writes it: NCH chunks of 128 rows x CC columns, each chunk row-major with
+// ROWB-byte rows, swizzled in 8-row atoms.
+template <int D>
+struct TileGeo {
+  static constexpr int CC = chunk_cols(D);
+  static constexpr int NCH = (D + CC - 1) / CC;
+  static constexpr int ROWB = CC * 2;
+  static constexpr int CHB = kTileRows * ROWB;
+  static constexpr int TILE = NCH * CHB;
+  static constexpr int SBO = 8 * ROWB;                // bytes between 8-row groups
+  static constexpr uint32_t LAYOUT = CC == 64 ? 2u : 4u;   // UMMA descriptor: 128B / 64B swizzle
+  static constexpr int KPC = CC / 16;                 // 16-wide K-steps per chunk
+};
+
+// Encodes a 4-D TMA map {d, rows, H, B} with a {chunk_cols(d), 128, 1, 1}
+// box and the matching swizzle.  Returns false if the driver rejects it.
 bool make_tile_map(CUtensorMap* map, const Tensor4& t, int d, int rows, int H, int B, bool bf16);
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);

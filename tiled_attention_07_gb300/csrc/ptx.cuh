@@ -225,23 +225,24 @@ __host__ __device__ constexpr uint32_t make_idesc_f16(bool bf16, int M, int N, b
          ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// Shared-memory matrix descriptor, 128-byte swizzle (the layout TMA writes with
-// CU_TENSOR_MAP_SWIZZLE_128B: rows of 128 bytes, 16-byte chunk c of row r
-// stored at chunk c ^ (r % 8), 8-row atoms of 1024 bytes; tile bases are
-// 1024-byte aligned).
+// Shared-memory matrix descriptor of a swizzled tile (the layouts TMA writes
+// with CU_TENSOR_MAP_SWIZZLE_128B / _64B: rows of 128 / 64 bytes, the 16-byte
+// chunk c of row r stored at c XOR (address bits of r), in 8-row atoms; tile
+// bases are 1024-byte aligned).
 //   bits 0-13  start address >> 4     bits 16-29 leading byte offset >> 4
 //   bits 32-45 stride byte offset >> 4   bits 46-47 version (1)
-//   bits 61-63 layout (2 = 128-byte swizzle)
-// K-major operand: SBO = distance between 8-row groups (1024); LBO unused.
-// MN-major operand: LBO = distance between 64-element column blocks,
-// SBO = distance between groups of 8 rows along K (1024).
-__device__ __forceinline__ uint64_t make_sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+//   bits 61-63 layout (2 = 128-byte swizzle, 4 = 64-byte swizzle)
+// K-major operand: SBO = distance between 8-row groups; LBO unused.
+// MN-major operand: LBO = distance between column chunks, SBO = distance
+// between groups of 8 rows along K.
+__device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                                               uint32_t layout) {
   uint64_t d = 0;
   d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
   d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
   d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
   d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
+  d |= (uint64_t)(layout & 7u) << 61;
   return d;
 }
 
