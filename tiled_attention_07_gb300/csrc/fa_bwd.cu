@@ -204,9 +204,12 @@ __device__ __forceinline__ void store16(uint8_t* dst, const uint32_t (&v)[16], f
 // ---------------------------------------------------------------------------
 // dK / dV: one CTA per (key tile, b, h)
 // ---------------------------------------------------------------------------
-// TMEM columns: [0,128) S^T -> P^T, [128,256) dP^T -> dS^T, [256,256+D) dV,
-// [384,384+D) dK.  Elementwise warps: warpgroup g = warp / 4 owns query
-// columns [64 g, 64 g + 64) of S^T / dP^T; warp % 4 selects the 32 key rows.
+// TMEM columns: [0,128) S^T, [128,256) dP^T -> dS^T, then dV and dK (D
+// columns each).  With d <= 96 a 64-column region after dK holds the 16-bit
+// P^T, so S^T_{i+1} is computed while the elementwise warps still work on
+// tile i; with d = 128 there is no room and P^T overwrites S^T.  Elementwise warps:
+// warpgroup g = warp / 4 owns query columns [32 g, 32 g + 32); warp % 4
+// selects the 32 key rows.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -214,9 +217,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                 const MainParams p) {
   using C = BwdCfg<D>;
   constexpr int NS = C::KV_NSTAGE;
-  // With d <= 96, P^T (64 columns of packed 16-bit pairs) gets TMEM columns of
-  // its own after dV and dK, so S^T_{i+1} can be computed while the
-  // elementwise warps still work on tile i.  Otherwise it overwrites S^T.
+  // kSepP: P^T has a 64-column region of its own (see above).
   constexpr bool kSepP = 256 + 2 * D + 64 <= 512;
   constexpr uint32_t kColDV = 256;
   constexpr uint32_t kColDK = kSepP ? 256 + D : 384;
@@ -237,15 +238,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   uint64_t* bar_acc = bar_ds + 1;     // dV, dK complete (one commit per issuer)
   uint64_t* bar_drain = bar_acc + 1;  // every MMA of both issuers complete
   uint64_t* bar_sfree = bar_drain + 1;  // S^T read into registers (separate-P^T layout)
-  uint64_t* bar_dvd = bar_sfree + 1;    // dV_i complete: the P^T columns are free again
+  uint64_t* bar_dvd = bar_sfree + 1;    // dV_i complete: P^T_i consumed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_dvd + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int BH = p.B * p.H;
-  // Heaviest key tiles first (for causal the first key tile sees every query).
-  const int kt = static_cast<int>(blockIdx.x / BH);
-  const int bh = static_cast<int>(blockIdx.x % BH);
+  // Heads in chunks sharing Q/dO through L2; inside a chunk the heaviest key
+  // tiles first (for causal the first key tile sees every query).
+  int kt, bh;
+  chunked_order(static_cast<int>(blockIdx.x), (p.Nk + kT - 1) / kT, BH, &kt, &bh);
   const int b = bh / p.H;
   const int h = bh % p.H;
   const int k0 = kt * kT;
@@ -509,9 +511,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 // ---------------------------------------------------------------------------
 // dQ: one CTA per (query tile, b, h)
 // ---------------------------------------------------------------------------
-// TMEM columns: [0,128) S, [128,256) dP -> dS, [256,256+D) dQ.  Elementwise
-// warps: warpgroup g owns key columns [32 g, 32 g + 32); warp % 4 selects
-// the 32 query rows.
+// TMEM columns: [0,128) S, [128,256) dP, [256,256+D) dQ, then 64 columns
+// for the 16-bit dS (A operand of the dQ MMA).  dS having columns of its own,
+// dP_{j+1} is issued as soon as dP_j is in registers.  Elementwise warps:
+// warpgroup g owns key columns [32 g, 32 g + 32); warp % 4 selects the 32
+// query rows.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -519,6 +523,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
               const MainParams p) {
   using C = BwdCfg<D>;
   constexpr int NS = C::Q_NSTAGE;
+  constexpr uint32_t kColDQ = 256;
+  constexpr uint32_t kColDS = 256 + (D + 31) / 32 * 32;
+  static_assert(kColDS + 64 <= 512, "TMEM budget");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
@@ -534,15 +541,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   uint64_t* bar_ds = bar_sfree + 1;   // dS written
   uint64_t* bar_acc = bar_ds + 1;     // dQ complete (one commit per issuer)
   uint64_t* bar_drain = bar_acc + 1;  // every MMA of both issuers complete
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_drain + 1);
+  uint64_t* bar_dpfree = bar_drain + 1;  // dP_j read into registers
+  uint64_t* bar_dqd = bar_dpfree + 1;    // dQ += dS_j K_j complete: dS_j consumed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_dqd + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int BH = p.B * p.H;
   const int nqt = (p.Nq + kT - 1) / kT;
-  // Heaviest query tiles first (for causal the last query tile sees every key).
-  const int qt = nqt - 1 - static_cast<int>(blockIdx.x / BH);
-  const int bh = static_cast<int>(blockIdx.x % BH);
+  // Heads in chunks sharing K/V through L2; inside a chunk the heaviest query
+  // tiles first (for causal the last query tile sees every key).
+  int rank, bh;
+  chunked_order(static_cast<int>(blockIdx.x), nqt, BH, &rank, &bh);
+  const int qt = nqt - 1 - rank;
   const int b = bh / p.H;
   const int h = bh % p.H;
   const int q0 = qt * kT;
@@ -561,6 +572,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     mbar_init(bar_ds, C::EW_WARPS);
     mbar_init(bar_acc, 2);
     mbar_init(bar_drain, 2);
+    mbar_init(bar_dpfree, C::EW_WARPS);
+    mbar_init(bar_dqd, 1);
     fence_mbar_init();
   }
   if (warp == C::MMA_WARP) {
@@ -621,12 +634,23 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           mma_nt<D>(tmem, sq, sk, idesc_nt);                // S_j = Q K_j^T
           umma_commit(bar_s);
         } else {
-          tc_fence_after();
-          mma_nt<D>(tmem + 128, sdo, sk + C::TILE, idesc_nt);   // dP_j = dO V_j^T
-          umma_commit(bar_dp);
+          if (jt == 0) {
+            tc_fence_after();
+            mma_nt<D>(tmem + 128, sdo, sk + C::TILE, idesc_nt);   // dP_0 = dO V_0^T
+            umma_commit(bar_dp);
+          }
+          if (jt + 1 < n_jt) {
+            const int s1 = (jt + 1) % NS;
+            mbar_wait(&bar_full[s1], ((jt + 1) / NS) & 1, p.err, 44);
+            mbar_wait(bar_dpfree, jt & 1, p.err, 50);   // dP_j read
+            tc_fence_after();
+            mma_nt<D>(tmem + 128, sdo, sst + s1 * C::Q_STAGE + C::TILE, idesc_nt);   // dP_{j+1}
+            umma_commit(bar_dp);
+          }
           mbar_wait(bar_ds, jt & 1, p.err, 46);
           tc_fence_after();
-          mma_tn<D>(tmem + 256, tmem + 128, sk, idesc_tn, jt > 0);  // dQ += dS_j K_j
+          mma_tn<D, true>(tmem + kColDQ, tmem + kColDS, sk, idesc_tn, jt > 0);  // dQ += dS_j K_j
+          umma_commit(bar_dqd);
         }
         umma_commit(&bar_empty[s]);
       }
@@ -645,6 +669,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t tS = tmem + lane_off + g * 32;
     const uint32_t tdP = tmem + lane_off + 128 + g * 32;
+    const uint32_t tdS = tmem + lane_off + kColDS + g * 16;
     const int64_t wrow = static_cast<int64_t>(bh) * p.Nqp + qrow;
     const float nLr = p.wsL[wrow];   // -L log2 e; -inf on padded rows
     const float Dr = p.wsD[wrow];
@@ -688,6 +713,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         uint32_t r[32];
         tmem_ld32(tdP, r);
         tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_dpfree);   // dP_j is in registers
         // dS = P o (dP - D)
         uint32_t pk[16];
 #pragma unroll
@@ -698,7 +726,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
                    a0, a1);
           pk[e] = pack2<BF16>(a0, a1);
         }
-        tmem_st16(tdP, pk);
+        if (jt > 0) {
+          mbar_wait(bar_dqd, (jt - 1) & 1, p.err, 51);   // dS_{j-1} consumed
+          tc_fence_after();
+        }
+        tmem_st16(tdS, pk);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -713,7 +745,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     }
     const bool valid = qrow < p.Nq;
     uint8_t* dst = const_cast<uint8_t*>(row_ptr(p.out0, p.o0_sb, p.o0_sh, p.o0_ss, b, h, qrow));
-    const uint32_t tacc = tmem + lane_off + 256;
+    const uint32_t tacc = tmem + lane_off + kColDQ;
 #pragma unroll
     for (int c = 0; c < D / 16; ++c) {
       if ((c & 3) != g) continue;

@@ -132,12 +132,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Work decode: heaviest query-tile pairs first (longest-processing-time
-  // order for causal), all (b, h) of one pair index next to each other.
+  // Work decode: heads in chunks sharing K/V through L2; inside a chunk the
+  // heaviest query-tile pairs first (longest-processing-time order for causal).
   const int BH = p.B * p.H;
-  const int lin = blockIdx.x;
-  const int pair = p.n_pairs - 1 - lin / BH;
-  const int bh = lin % BH;
+  int rank, bh;
+  chunked_order(static_cast<int>(blockIdx.x), p.n_pairs, BH, &rank, &bh);
+  const int pair = p.n_pairs - 1 - rank;
   const int b = bh / p.H;
   const int h = bh % p.H;
   const int q0 = pair * (kNQT * kBM);

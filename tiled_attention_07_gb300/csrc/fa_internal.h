@@ -60,6 +60,22 @@ struct TileGeo {
   static constexpr int KPC = CC / 16;                 // 16-wide K-steps per chunk
 };
 
+// Work order of the attention kernels: one block per (tile, head).  Heads
+// are taken in chunks of kHeadChunk so that the blocks that run at the same
+// time share K/V (or Q/dO) tiles through L2; inside a chunk the tiles go in
+// the order 0, 1, 2, ... of `rank` (the caller maps rank 0 to its heaviest
+// tile), with all heads of the chunk at one rank next to each other.
+constexpr int kHeadChunk = 8;
+
+__host__ __device__ inline void chunked_order(int lin, int n_tiles, int BH, int* rank, int* bh) {
+  const int per_chunk = kHeadChunk * n_tiles;
+  const int chunk = lin / per_chunk;
+  const int heads = BH - chunk * kHeadChunk < kHeadChunk ? BH - chunk * kHeadChunk : kHeadChunk;
+  const int r = lin - chunk * per_chunk;
+  *rank = r / heads;
+  *bh = chunk * kHeadChunk + r % heads;
+}
+
 // Encodes a 4-D TMA map {d, rows, H, B} with a {chunk_cols(d), 128, 1, 1}
 // box and the matching swizzle.  Returns false if the driver rejects it.
 bool make_tile_map(CUtensorMap* map, const Tensor4& t, int d, int rows, int H, int B, bool bf16);
