@@ -148,11 +148,12 @@ __device__ __forceinline__ uint32_t split_a_col(int ks) { return (ks >> 1) * 32 
 template <int D>
 __device__ __forceinline__ void mma_nt(uint32_t d_tmem, uint32_t a_addr, uint32_t b_addr, uint32_t idesc) {
   using G = TileGeo<D>;
+  const uint64_t ad0 = make_sdesc(a_addr, 16, G::SBO, G::LAYOUT);
+  const uint64_t bd0 = make_sdesc(b_addr, 16, G::SBO, G::LAYOUT);
 #pragma unroll
   for (int ks = 0; ks < D / 16; ++ks) {
     const uint32_t off = (ks / G::KPC) * G::CHB + (ks % G::KPC) * 32;
-    umma_ss(d_tmem, make_sdesc(a_addr + off, 16, G::SBO, G::LAYOUT), make_sdesc(b_addr + off, 16, G::SBO, G::LAYOUT),
-            idesc, ks > 0);
+    umma_ss(d_tmem, desc_add(ad0, off), desc_add(bd0, off), idesc, ks > 0);
   }
 }
 
@@ -163,11 +164,11 @@ template <int D, bool kContiguousA = false>
 __device__ __forceinline__ void mma_tn(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_addr, uint32_t idesc,
                                        bool acc) {
   using G = TileGeo<D>;
+  const uint64_t bd0 = make_sdesc(b_addr, G::CHB, G::SBO, G::LAYOUT);
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
     const uint32_t acol = kContiguousA ? static_cast<uint32_t>(ks * 8) : split_a_col(ks);
-    umma_ts(d_tmem, a_tmem + acol, make_sdesc(b_addr + ks * 16 * G::ROWB, G::CHB, G::SBO, G::LAYOUT), idesc,
-            (acc || ks > 0) ? 1u : 0u);
+    umma_ts(d_tmem, a_tmem + acol, desc_add(bd0, ks * 16 * G::ROWB), idesc, (acc || ks > 0) ? 1u : 0u);
   }
 }
 

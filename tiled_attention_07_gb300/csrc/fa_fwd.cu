@@ -25,7 +25,9 @@
 // softmax runs on S_0 the tensor cores compute PV and the next S of tile 1,
 // and the other way round.
 // O is rescaled in TMEM only when a row's running max grows by more than
-// 2^8 (the stale max stays exact because l uses the same max).
+// 2^8 (the stale max stays exact because l uses the same max); in the common
+// case the exponentials are taken against the running max in the same pass
+// that finds the tile max, and the tile is redone only when a max jumped.
 // Causal: tiles above the diagonal are never loaded or computed; only the
 // diagonal tile and the ragged key tail are masked.
 #include "fa_internal.h"
@@ -85,12 +87,13 @@ __device__ __forceinline__ void issue_s(uint32_t tmem, uint32_t sq_addr, uint32_
   using G = TileGeo<D>;
   constexpr uint32_t idesc = make_idesc_f16(BF16, kBM, kBN, false, false);
   constexpr int TILE = FwdCfg<D>::TILE;
+  const uint64_t ad0 = make_sdesc(sq_addr + t * TILE, 16, G::SBO, G::LAYOUT);
+  const uint64_t bd0 = make_sdesc(skv_addr + slot * TILE, 16, G::SBO, G::LAYOUT);
+  const uint32_t d = tmem + t * 128;
 #pragma unroll
   for (int ks = 0; ks < D / 16; ++ks) {
     const uint32_t off = (ks / G::KPC) * G::CHB + (ks % G::KPC) * 32;
-    const uint64_t ad = make_sdesc(sq_addr + t * TILE + off, 16, G::SBO, G::LAYOUT);
-    const uint64_t bd = make_sdesc(skv_addr + slot * TILE + off, 16, G::SBO, G::LAYOUT);
-    umma_ss(tmem + t * 128, ad, bd, idesc, ks > 0);
+    umma_ss(d, desc_add(ad0, off), desc_add(bd0, off), idesc, ks > 0);
   }
 }
 
@@ -102,11 +105,12 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t skv_addr, int t
   using G = TileGeo<D>;
   constexpr uint32_t idesc = make_idesc_f16(BF16, kBM, D, false, true);
   constexpr int TILE = FwdCfg<D>::TILE;
+  const uint64_t bd0 = make_sdesc(skv_addr + slot * TILE, G::CHB, G::SBO, G::LAYOUT);
+  const uint32_t d = tmem + 256 + t * 128;
+  const uint32_t a = tmem + t * 128;
 #pragma unroll
-  for (int ks = 0; ks < kBN / 16; ++ks) {
-    const uint64_t bd = make_sdesc(skv_addr + slot * TILE + ks * 16 * G::ROWB, G::CHB, G::SBO, G::LAYOUT);
-    umma_ts(tmem + 256 + t * 128, tmem + t * 128 + ks * 8, bd, idesc, (acc || ks > 0) ? 1u : 0u);
-  }
+  for (int ks = 0; ks < kBN / 16; ++ks)
+    umma_ts(d, a + ks * 8, desc_add(bd0, ks * 16 * G::ROWB), idesc, (acc || ks > 0) ? 1u : 0u);
 }
 
 template <int D, bool BF16>
@@ -307,23 +311,61 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         for (int c = 0; c < kBN; ++c)
           if (kbase + c >= lim) s[c] = -CUDART_INF_F;
       }
-      // row max: eight independent chains of 3-input max
-      float mc[8];
+      const uint64_t cs2 = f2pack(cs, cs);
+      bool done = false;
+      if (j > 0) {
+        // Common case: exp2 against the running max m (any score up to
+        // m + 8 gives p <= 2^8), finding the tile max in the same pass.  If a
+        // row's max grew by more than 8, the tile is redone below with a new
+        // max; otherwise this is exactly the result of the redo.
+        const uint64_t nm2 = f2pack(-m, -m);
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+        float mc[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mc[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+        for (int i = 0; i < 8; ++i) mc[i] = -CUDART_INF_F;
 #pragma unroll
-      for (int c = 16; c < kBN; c += 16) {
+        for (int i = 0; i < kBN / 32; ++i) {
+          uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mc[i] = fmax3(mc[i], s[c + 2 * i], s[c + 2 * i + 1]);
+          for (int e = 0; e < 16; ++e) {
+            const int c = i * 32 + 2 * e;
+            mc[e & 7] = fmax3(mc[e & 7], s[c], s[c + 1]);
+            float x0, x1;
+            f2unpack(ffma2(f2pack(s[c], s[c + 1]), cs2, nm2), x0, x1);
+            const float p0 = ex2_approx(x0);
+            const float p1 = ex2_approx(x1);
+            acc[e & 3] = fadd2(acc[e & 3], f2pack(p0, p1));
+            pk[e] = pack2<BF16>(p0, p1);
+          }
+          tmem_st16(tS + i * 16, pk);
+        }
+        const float mx = fmax3(fmax3(mc[0], mc[1], mc[2]), fmax3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
+        const bool need = mx * cs > m + kRescaleLog2;
+        if (!__any_sync(0xffffffffu, need)) {
+          float a0, a1;
+          f2unpack(fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3])), a0, a1);
+          l += a0 + a1;
+          done = true;
+        }
       }
-      const float mx = fmax3(fmax3(mc[0], mc[1], mc[2]), fmax3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
-      const float m_tile = mx * cs;
-
-      if (j == 0) {
-        m = m_tile;
-      } else {
-        const bool need = m_tile > m + kRescaleLog2;
-        if (__any_sync(0xffffffffu, need)) {
+      if (!done) {
+        // First tile, or a running max grew by more than 2^8 in this warp:
+        // new max, O and l rescaled, p recomputed.
+        // row max: eight independent chains of 3-input max
+        float mc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mc[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+        for (int c = 16; c < kBN; c += 16) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mc[i] = fmax3(mc[i], s[c + 2 * i], s[c + 2 * i + 1]);
+        }
+        const float mx = fmax3(fmax3(mc[0], mc[1], mc[2]), fmax3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
+        const float m_tile = mx * cs;
+        if (j == 0) {
+          m = m_tile;
+        } else {
+          const bool need = m_tile > m + kRescaleLog2;
           const float m_new = need ? m_tile : m;
           const float alpha = ex2_approx(m - m_new);
           m = m_new;
@@ -344,34 +386,29 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
             tmem_st16(tO + c * 16, o);
           }
         }
-      }
-      const float mb = (m == -CUDART_INF_F) ? 0.f : m;
+        const float mb = (m == -CUDART_INF_F) ? 0.f : m;
 
-      // p = exp2(c s - m) two at a time (packed FFMA), row sum in four
-      // independent packed accumulators
-      const uint64_t cs2 = f2pack(cs, cs);
-      const uint64_t nm2 = f2pack(-mb, -mb);
-      uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+        // p = exp2(c s - m) two at a time (packed FFMA), row sum in four
+        // independent packed accumulators
+        const uint64_t nm2 = f2pack(-mb, -mb);
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-      for (int i = 0; i < kBN / 32; ++i) {
-        uint32_t pk[16];
+        for (int i = 0; i < kBN / 32; ++i) {
+          uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int c = i * 32 + 2 * e;
-          float x0, x1;
-          f2unpack(ffma2(f2pack(s[c], s[c + 1]), cs2, nm2), x0, x1);
-          const float p0 = ex2_approx(x0);
-          const float p1 = ex2_approx(x1);
-          acc[e & 3] = fadd2(acc[e & 3], f2pack(p0, p1));
-          pk[e] = pack2<BF16>(p0, p1);
+          for (int e = 0; e < 16; ++e) {
+            const int c = i * 32 + 2 * e;
+            float x0, x1;
+            f2unpack(ffma2(f2pack(s[c], s[c + 1]), cs2, nm2), x0, x1);
+            const float p0 = ex2_approx(x0);
+            const float p1 = ex2_approx(x1);
+            acc[e & 3] = fadd2(acc[e & 3], f2pack(p0, p1));
+            pk[e] = pack2<BF16>(p0, p1);
+          }
+          tmem_st16(tS + i * 16, pk);
         }
-        tmem_st16(tS + i * 16, pk);
-      }
-      {
-        float a0, a1, b0, b1;
+        float a0, a1;
         f2unpack(fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3])), a0, a1);
-        (void)b0;
-        (void)b1;
         l += a0 + a1;
       }
       tmem_wait_st();

@@ -246,6 +246,20 @@ __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo_byte
   return d;
 }
 
+// The descriptor of the same operand advanced by `bytes` (a multiple of 16):
+// one 32-bit add on the start-address field, which cannot carry out of its
+// 14 bits for shared-memory addresses below 256 KB.  Keeps the per-MMA
+// instruction count of the issuing thread small: it shares its issue slots
+// with busy softmax / elementwise warps.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) {
+  uint32_t lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(d));
+  lo += bytes >> 4;
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+
 // ---------------------------------------------------------------------------
 // TMEM <-> registers (32x32b shape: thread t of the warp holds lane
 // (32 * (warp % 4) + t); consecutive registers are consecutive columns)
