@@ -153,7 +153,7 @@ __device__ __forceinline__ void mma_nt(uint32_t d_tmem, uint32_t a_addr, uint32_
 #pragma unroll
   for (int ks = 0; ks < D / 16; ++ks) {
     const uint32_t off = (ks / G::KPC) * G::CHB + (ks % G::KPC) * 32;
-    umma_ss(d_tmem, desc_add(ad0, off), desc_add(bd0, off), idesc, ks > 0);
+    if (elect_one()) umma_ss(d_tmem, desc_add(ad0, off), desc_add(bd0, off), idesc, ks > 0);
   }
 }
 
@@ -168,7 +168,7 @@ __device__ __forceinline__ void mma_tn(uint32_t d_tmem, uint32_t a_tmem, uint32_
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
     const uint32_t acol = kContiguousA ? static_cast<uint32_t>(ks * 8) : split_a_col(ks);
-    umma_ts(d_tmem, a_tmem + acol, desc_add(bd0, ks * 16 * G::ROWB), idesc, (acc || ks > 0) ? 1u : 0u);
+    if (elect_one()) umma_ts(d_tmem, a_tmem + acol, desc_add(bd0, ks * 16 * G::ROWB), idesc, (acc || ks > 0) ? 1u : 0u);
   }
 }
 
@@ -318,18 +318,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     // dK, so that one issuer's barrier polls are covered by the other's MMAs.
     // Each releases every stage once (the empty barriers count two).
     const bool issuer_a = warp == C::MMA_WARP;
-    if (lane == 0 && n_it > 0) {
+    if (n_it > 0) {
       constexpr uint32_t idesc_nt = make_idesc_f16(BF16, kT, kT, false, false);
       constexpr uint32_t idesc_tn = make_idesc_f16(BF16, kT, D, false, true);
       const uint32_t sk = smem_u32(sK);
       const uint32_t sv = smem_u32(sV);
       const uint32_t sst = smem_u32(sStage);
       mbar_wait(bar_kv, 0, p.err, 22);
+      __syncwarp();
       for (int it = 0; it < n_it; ++it) {
         const int s = it % NS;
         const uint32_t sq = sst + s * C::KV_STAGE;
         const uint32_t sdo = sq + C::TILE;
         mbar_wait(&bar_full[s], (it / NS) & 1, p.err, 23);
+        __syncwarp();
         tc_fence_after();
         if (issuer_a) {
           if (kSepP) {
@@ -337,42 +339,45 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             // as the elementwise warps hold S^T_i in registers.
             if (it == 0) {
               mma_nt<D>(tmem, sk, sq, idesc_nt);          // S^T_0 = K Q_0^T
-              umma_commit(bar_s);
+              if (elect_one()) umma_commit(bar_s);
             }
             if (it + 1 < n_it) {
               const int s1 = (it + 1) % NS;
               mbar_wait(&bar_full[s1], ((it + 1) / NS) & 1, p.err, 25);
               mbar_wait(bar_sfree, it & 1, p.err, 31);
+              __syncwarp();
               tc_fence_after();
               mma_nt<D>(tmem, sk, sst + s1 * C::KV_STAGE, idesc_nt);   // S^T_{i+1}
-              umma_commit(bar_s);
+              if (elect_one()) umma_commit(bar_s);
             }
             mbar_wait(bar_pt, it & 1, p.err, 24);
+            __syncwarp();
             tc_fence_after();
             mma_tn<D, true>(tmem + kColDV, tmem + kColP, sdo, idesc_tn, it > 0);  // dV += P^T_i dO_i
-            umma_commit(bar_dvd);
+            if (elect_one()) umma_commit(bar_dvd);
           } else {
             mma_nt<D>(tmem, sk, sq, idesc_nt);            // S^T_i = K Q_i^T
-            umma_commit(bar_s);
+            if (elect_one()) umma_commit(bar_s);
             mbar_wait(bar_pt, it & 1, p.err, 24);
+            __syncwarp();
             tc_fence_after();
             mma_tn<D>(tmem + kColDV, tmem, sdo, idesc_tn, it > 0);  // dV += P^T_i dO_i
           }
         } else {
           mma_nt<D>(tmem + 128, sv, sdo, idesc_nt);       // dP^T_i = V dO_i^T
-          umma_commit(bar_dp);
+          if (elect_one()) umma_commit(bar_dp);
           mbar_wait(bar_ds, it & 1, p.err, 26);
+          __syncwarp();
           tc_fence_after();
           mma_tn<D>(tmem + kColDK, tmem + 128, sq, idesc_tn, it > 0);  // dK += dS^T_i Q_i
         }
-        umma_commit(&bar_empty[s]);
+        if (elect_one()) umma_commit(&bar_empty[s]);
       }
-      umma_commit(bar_acc);
+      if (elect_one()) umma_commit(bar_acc);
     }
-    if (lane == 0) {
-      umma_commit(bar_drain);
-      mbar_wait_drain(bar_drain, 0);
-    }
+    if (elect_one()) umma_commit(bar_drain);
+    __syncwarp();
+    mbar_wait_drain(bar_drain, 0);
   } else {
     // ------------------------------------------------------- elementwise
     // Warpgroup g owns query columns [32 g, 32 g + 32) of S^T / dP^T; warp % 4
@@ -618,7 +623,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     // Two issuers: A (warp 9) computes S_j, B (warp 10) dP_j and dQ; each
     // releases every stage once (the empty barriers count two).
     const bool issuer_a = warp == C::MMA_WARP;
-    if (lane == 0 && n_jt > 0) {
+    if (n_jt > 0) {
       constexpr uint32_t idesc_nt = make_idesc_f16(BF16, kT, kT, false, false);
       constexpr uint32_t idesc_tn = make_idesc_f16(BF16, kT, D, false, true);
       const uint32_t sq = smem_u32(sQ);
@@ -629,38 +634,41 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         const int s = jt % NS;
         const uint32_t sk = sst + s * C::Q_STAGE;
         mbar_wait(&bar_full[s], (jt / NS) & 1, p.err, 43);
+        __syncwarp();
         if (issuer_a) {
           if (jt > 0) mbar_wait(bar_sfree, (jt - 1) & 1, p.err, 45);   // S_{j-1} read
+          __syncwarp();
           tc_fence_after();
           mma_nt<D>(tmem, sq, sk, idesc_nt);                // S_j = Q K_j^T
-          umma_commit(bar_s);
+          if (elect_one()) umma_commit(bar_s);
         } else {
           if (jt == 0) {
             tc_fence_after();
             mma_nt<D>(tmem + 128, sdo, sk + C::TILE, idesc_nt);   // dP_0 = dO V_0^T
-            umma_commit(bar_dp);
+            if (elect_one()) umma_commit(bar_dp);
           }
           if (jt + 1 < n_jt) {
             const int s1 = (jt + 1) % NS;
             mbar_wait(&bar_full[s1], ((jt + 1) / NS) & 1, p.err, 44);
             mbar_wait(bar_dpfree, jt & 1, p.err, 50);   // dP_j read
+            __syncwarp();
             tc_fence_after();
             mma_nt<D>(tmem + 128, sdo, sst + s1 * C::Q_STAGE + C::TILE, idesc_nt);   // dP_{j+1}
-            umma_commit(bar_dp);
+            if (elect_one()) umma_commit(bar_dp);
           }
           mbar_wait(bar_ds, jt & 1, p.err, 46);
+          __syncwarp();
           tc_fence_after();
           mma_tn<D, true>(tmem + kColDQ, tmem + kColDS, sk, idesc_tn, jt > 0);  // dQ += dS_j K_j
-          umma_commit(bar_dqd);
+          if (elect_one()) umma_commit(bar_dqd);
         }
-        umma_commit(&bar_empty[s]);
+        if (elect_one()) umma_commit(&bar_empty[s]);
       }
-      umma_commit(bar_acc);
+      if (elect_one()) umma_commit(bar_acc);
     }
-    if (lane == 0) {
-      umma_commit(bar_drain);
-      mbar_wait_drain(bar_drain, 0);
-    }
+    if (elect_one()) umma_commit(bar_drain);
+    __syncwarp();
+    mbar_wait_drain(bar_drain, 0);
   } else {
     // Warpgroup g owns key columns [32 g, 32 g + 32) of S / dP; warp % 4
     // selects the 32 query rows (TMEM lanes) of its thread.

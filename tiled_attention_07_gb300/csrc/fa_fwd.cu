@@ -14,11 +14,16 @@
 //   warps 4-7  the same for query tile 1
 //   warp  8    TMA producer: Q tiles once, then K_j, V_j through an
 //              mbarrier ring of NSTAGE shared-memory slots
-//   warps 9-10 tcgen05.mma issuers, one thread per query tile (warp 9 also
-//              allocates TMEM).  Two issuing threads keep the tensor pipe fed:
-//              the issue of tcgen05.mma runs at most about one MMA ahead of its
+//   warps 9-10 tcgen05.mma issuers, one warp per query tile (warp 9 also
+//              allocates TMEM).  Two issuers keep the tensor pipe fed: the
+//              issue of tcgen05.mma runs at most about one MMA ahead of its
 //              execution, so every barrier poll by an issuer leaves a bubble
-//              that only the other issuer's MMAs can fill.
+//              that only the other issuer's MMAs can fill.  The whole warp
+//              runs the issue loop (descriptors are warp-uniform) and one
+//              elected lane issues each MMA: an issuing warp shares its
+//              sub-partition's issue slots with two busy softmax warps, and
+//              in this form it keeps the MMA rate they would otherwise cut
+//              by a third.
 // Tensor memory (512 columns x 128 lanes): S_t at column 128*t (fp32 scores,
 // overwritten in place by the 16-bit P_t that feeds the PV MMA as its A
 // operand), O_t at column 256 + 128*t (fp32 accumulator).  While tile 0's
@@ -93,7 +98,7 @@ __device__ __forceinline__ void issue_s(uint32_t tmem, uint32_t sq_addr, uint32_
 #pragma unroll
   for (int ks = 0; ks < D / 16; ++ks) {
     const uint32_t off = (ks / G::KPC) * G::CHB + (ks % G::KPC) * 32;
-    umma_ss(d, desc_add(ad0, off), desc_add(bd0, off), idesc, ks > 0);
+    if (elect_one()) umma_ss(d, desc_add(ad0, off), desc_add(bd0, off), idesc, ks > 0);
   }
 }
 
@@ -110,7 +115,7 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t skv_addr, int t
   const uint32_t a = tmem + t * 128;
 #pragma unroll
   for (int ks = 0; ks < kBN / 16; ++ks)
-    umma_ts(d, a + ks * 8, desc_add(bd0, ks * 16 * G::ROWB), idesc, (acc || ks > 0) ? 1u : 0u);
+    if (elect_one()) umma_ts(d, a + ks * 8, desc_add(bd0, ks * 16 * G::ROWB), idesc, (acc || ks > 0) ? 1u : 0u);
 }
 
 template <int D, bool BF16>
@@ -191,7 +196,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         for (int c = 0; c < C::G::NCH; ++c)
           tma_load_4d(sQ + t * C::TILE + c * C::G::CHB, &tmQ, &bar_q[t], c * C::G::CC, q0 + t * kBM, h, b);
       }
-      // K_0, V_0, K_1, V_1, ... : the order the MMA thread consumes them in.
+      // K_0, V_0, K_1, V_1, ... : the order the MMA issuers consume them in.
       // A slot is refilled only after its previous fill has landed (even if
       // a consumer that gave up released it early), so each slot has at most
       // one copy in flight and one pending expect-tx phase.  A give-up stops
@@ -232,7 +237,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     // both releases of one use of a slot come before any release of its next
     // use (the empty barriers count two).
     const int t = warp - C::MMA_WARP;
-    if (lane == 0 && n_max > 0) {
+    if (n_max > 0) {
       const uint32_t sq_addr = smem_u32(sQ);
       const uint32_t skv_addr = smem_u32(sKV);
       const int nt = nkt[t];
@@ -240,13 +245,16 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       if (nt > 0) mbar_wait(&bar_q[t], 0, p.err, 2);
       mbar_wait(&bar_full[0], 0, p.err, 3);
       if (t == 1) mbar_wait(&bar_turn[1], 0, p.err, 11);
+      __syncwarp();
       if (nt > 0) {
         tc_fence_after();
         issue_s<D, BF16>(tmem, sq_addr, skv_addr, t, 0);
       }
-      mbar_arrive(&bar_turn[1 - t]);
-      if (nt > 0) umma_commit(&bar_s[t]);
-      umma_commit(&bar_empty[0]);
+      if (elect_one()) {
+        mbar_arrive(&bar_turn[1 - t]);
+        if (nt > 0) umma_commit(&bar_s[t]);
+        umma_commit(&bar_empty[0]);
+      }
       for (int j = 0; j < n_max; ++j) {
         const int fv = 2 * j + 1;            // fill index of V_j
         const int fk = 2 * j + 2;            // fill index of K_{j+1}
@@ -257,17 +265,21 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         if (pv) mbar_wait(&bar_p[t], j & 1, p.err, 5);
         // turn: G(0,j) follows G(1,j-1), G(1,j) follows G(0,j)
         mbar_wait(&bar_turn[t], (t == 0 ? j : j + 1) & 1, p.err, 12);
+        __syncwarp();
         tc_fence_after();
         if (pv) issue_pv<D, BF16>(tmem, skv_addr, t, fv % C::NSTAGE, j > 0);
         if (sn) issue_s<D, BF16>(tmem, sq_addr, skv_addr, t, fk % C::NSTAGE);
-        mbar_arrive(&bar_turn[1 - t]);
-        if (pv && !sn) umma_commit(&bar_o[t]);   // last PV of this tile
-        if (sn) umma_commit(&bar_s[t]);
-        umma_commit(&bar_empty[fv % C::NSTAGE]);
-        if (j + 1 < n_max) umma_commit(&bar_empty[fk % C::NSTAGE]);
+        if (elect_one()) {
+          mbar_arrive(&bar_turn[1 - t]);
+          if (pv && !sn) umma_commit(&bar_o[t]);   // last PV of this tile
+          if (sn) umma_commit(&bar_s[t]);
+          umma_commit(&bar_empty[fv % C::NSTAGE]);
+          if (j + 1 < n_max) umma_commit(&bar_empty[fk % C::NSTAGE]);
+        }
       }
       // Drain: every MMA of both issuers has completed before TMEM is freed.
-      umma_commit(bar_drain);
+      if (elect_one()) umma_commit(bar_drain);
+      __syncwarp();
       mbar_wait_drain(bar_drain, 0);
     }
   } else {
