@@ -48,6 +48,8 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--source-hash", default=None, metavar="KERNEL",
+                    help="print the source hash that a traffic line for KERNEL must carry, and exit")
     return ap.parse_args(argv)
 
 
@@ -146,16 +148,38 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+#: Sources each kernel is compiled from (a change to any of them makes an
+#: earlier DRAM-traffic capture of that kernel stale).
+KERNEL_SOURCES = {
+    "fwd": ("fa_fwd.cu", "ptx.cuh", "fa_internal.h"),
+    "bwd_pre": ("fa_bwd.cu", "ptx.cuh", "fa_internal.h"),
+    "bwd_dkdv": ("fa_bwd.cu", "ptx.cuh", "fa_internal.h"),
+    "bwd_dq": ("fa_bwd.cu", "ptx.cuh", "fa_internal.h"),
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """Short SHA-256 of the CUDA sources `kernel` is built from."""
+    import hashlib
+
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "tiled_attention_07_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def committed_traffic(kernel: str):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary, if any
-    (a line ``traffic_bytes_per_launch <kernel> <bytes> <source-hash>``)."""
+    """DRAM bytes per launch of `kernel` from the committed ncu summary
+    (a line ``traffic_bytes_per_launch <kernel> <bytes> <source-hash>``), or
+    None if there is none or the kernel's sources changed since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.md")
     try:
         with open(path) as f:
             for line in f:
                 parts = line.split()
-                if len(parts) >= 3 and parts[0] == "traffic_bytes_per_launch" and parts[1] == kernel:
-                    return float(parts[2])
+                if len(parts) >= 4 and parts[0] == "traffic_bytes_per_launch" and parts[1] == kernel:
+                    return float(parts[2]) if parts[3] == kernel_source_hash(kernel) else None
     except OSError:
         pass
     return None
@@ -425,6 +449,9 @@ def run_reference(args):
 
 def main(argv=None):
     args = parse_args(argv)
+    if args.source_hash:
+        print(kernel_source_hash(args.source_hash))
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
