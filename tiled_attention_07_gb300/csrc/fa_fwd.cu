@@ -49,6 +49,10 @@ constexpr int kBM = 128;          // query rows per tile
 constexpr int kBN = 128;          // keys per tile
 constexpr int kNQT = 2;           // query tiles per CTA
 constexpr float kRescaleLog2 = 8.0f;
+// A row sum of p = exp2(c s - m) at most 2^kRescaleLog2 bounds every p of the
+// row by the same, i.e. its max grew by at most kRescaleLog2.
+constexpr float kFastSumBound = 256.0f;
+static_assert(kFastSumBound == (1 << static_cast<int>(kRescaleLog2)), "keep the two bounds in step");
 
 template <int D>
 struct FwdCfg {
@@ -85,37 +89,65 @@ __device__ __forceinline__ int key_tiles(int r0, int Nq, int Nk, int causal) {
   return n;
 }
 
-// S_t = Q_t K^T : M = 128 queries, N = 128 keys, K = D (16 per MMA), both
-// operands K-major.
+// Epilogue of one query row: O = O_acc / l to 16-bit (16-byte stores) and
+// LSE = ln(sum_j exp(sm_scale q.k_j)) = ln 2 * (m + log2 l); rows >= Nq
+// store nothing.
 template <int D, bool BF16>
-__device__ __forceinline__ void issue_s(uint32_t tmem, uint32_t sq_addr, uint32_t skv_addr, int t, int slot) {
+__device__ __forceinline__ void store_o_lse(const FwdParams& p, uint32_t tO, int b, int h, int qrow, float m,
+                                            float l) {
+  const float inv_l = 1.f / l;
+  const bool valid = qrow < p.Nq;
+  uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
+                  2 * (static_cast<int64_t>(b) * p.o_sb + static_cast<int64_t>(h) * p.o_sh +
+                       static_cast<int64_t>(qrow) * p.o_ss);
+#pragma unroll
+  for (int c = 0; c < D / 16; ++c) {
+    uint32_t o[16];
+    tmem_ld16(tO + c * 16, o);
+    tmem_wait_ld();
+    uint4 w0, w1;
+    w0.x = pack2<BF16>(__uint_as_float(o[0]) * inv_l, __uint_as_float(o[1]) * inv_l);
+    w0.y = pack2<BF16>(__uint_as_float(o[2]) * inv_l, __uint_as_float(o[3]) * inv_l);
+    w0.z = pack2<BF16>(__uint_as_float(o[4]) * inv_l, __uint_as_float(o[5]) * inv_l);
+    w0.w = pack2<BF16>(__uint_as_float(o[6]) * inv_l, __uint_as_float(o[7]) * inv_l);
+    w1.x = pack2<BF16>(__uint_as_float(o[8]) * inv_l, __uint_as_float(o[9]) * inv_l);
+    w1.y = pack2<BF16>(__uint_as_float(o[10]) * inv_l, __uint_as_float(o[11]) * inv_l);
+    w1.z = pack2<BF16>(__uint_as_float(o[12]) * inv_l, __uint_as_float(o[13]) * inv_l);
+    w1.w = pack2<BF16>(__uint_as_float(o[14]) * inv_l, __uint_as_float(o[15]) * inv_l);
+    if (valid) {
+      reinterpret_cast<uint4*>(orow + c * 32)[0] = w0;
+      reinterpret_cast<uint4*>(orow + c * 32)[1] = w1;
+    }
+  }
+  if (valid) p.lse[(static_cast<int64_t>(b) * p.H + h) * p.Nq + qrow] = (m + log2f(l)) * 0.69314718055994531f;
+}
+
+// S = Q_t K_j^T into TMEM columns [d_tmem, d_tmem + 128): M = 128 queries,
+// N = 128 keys, K = D (16 per MMA), both operands K-major in shared memory.
+template <int D, bool BF16>
+__device__ __forceinline__ void issue_s(uint32_t d_tmem, uint32_t q_addr, uint32_t k_addr) {
   using G = TileGeo<D>;
   constexpr uint32_t idesc = make_idesc_f16(BF16, kBM, kBN, false, false);
-  constexpr int TILE = FwdCfg<D>::TILE;
-  const uint64_t ad0 = make_sdesc(sq_addr + t * TILE, 16, G::SBO, G::LAYOUT);
-  const uint64_t bd0 = make_sdesc(skv_addr + slot * TILE, 16, G::SBO, G::LAYOUT);
-  const uint32_t d = tmem + t * 128;
+  const uint64_t ad0 = make_sdesc(q_addr, 16, G::SBO, G::LAYOUT);
+  const uint64_t bd0 = make_sdesc(k_addr, 16, G::SBO, G::LAYOUT);
 #pragma unroll
   for (int ks = 0; ks < D / 16; ++ks) {
     const uint32_t off = (ks / G::KPC) * G::CHB + (ks % G::KPC) * 32;
-    if (elect_one()) umma_ss(d, desc_add(ad0, off), desc_add(bd0, off), idesc, ks > 0);
+    if (elect_one()) umma_ss(d_tmem, desc_add(ad0, off), desc_add(bd0, off), idesc, ks > 0);
   }
 }
 
-// O_t += P_t V : M = 128 queries, N = D, K = 128 keys (16 per MMA); P_t
-// (16-bit, two per column) sits in TMEM columns [128 t, 128 t + 64), V is the
-// MN-major B operand.
+// O_t (+)= P V_j : M = 128 queries, N = D, K = 128 keys (16 per MMA).  P is
+// 16-bit, two per TMEM column, in columns [p_tmem, p_tmem + 64); V is the
+// MN-major B operand in shared memory.
 template <int D, bool BF16>
-__device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t skv_addr, int t, int slot, bool acc) {
+__device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint32_t v_addr, bool acc) {
   using G = TileGeo<D>;
   constexpr uint32_t idesc = make_idesc_f16(BF16, kBM, D, false, true);
-  constexpr int TILE = FwdCfg<D>::TILE;
-  const uint64_t bd0 = make_sdesc(skv_addr + slot * TILE, G::CHB, G::SBO, G::LAYOUT);
-  const uint32_t d = tmem + 256 + t * 128;
-  const uint32_t a = tmem + t * 128;
+  const uint64_t bd0 = make_sdesc(v_addr, G::CHB, G::SBO, G::LAYOUT);
 #pragma unroll
   for (int ks = 0; ks < kBN / 16; ++ks)
-    if (elect_one()) umma_ts(d, a + ks * 8, desc_add(bd0, ks * 16 * G::ROWB), idesc, (acc || ks > 0) ? 1u : 0u);
+    if (elect_one()) umma_ts(o_tmem, p_tmem + ks * 8, desc_add(bd0, ks * 16 * G::ROWB), idesc, (acc || ks > 0) ? 1u : 0u);
 }
 
 template <int D, bool BF16>
@@ -132,7 +164,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   uint64_t* bar_full = bar_q + kNQT;                // [NSTAGE]
   uint64_t* bar_empty = bar_full + C::NSTAGE;       // [NSTAGE]
   uint64_t* bar_s = bar_empty + C::NSTAGE;          // [kNQT] S_t ready
-  uint64_t* bar_p = bar_s + kNQT;                   // [kNQT] P_t written (128 arrivals)
+  uint64_t* bar_p = bar_s + kNQT;                   // [kNQT] P_t written (one arrival per softmax warp)
   uint64_t* bar_o = bar_p + kNQT;                   // [kNQT] PV_t complete
   uint64_t* bar_turn = bar_o + kNQT;                // [kNQT] issuer t may issue its next group
   uint64_t* bar_drain = bar_turn + kNQT;            // [1]
@@ -163,7 +195,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     for (int t = 0; t < kNQT; ++t) {
       mbar_init(&bar_q[t], 1);
       mbar_init(&bar_s[t], 1);
-      mbar_init(&bar_p[t], 128);
+      mbar_init(&bar_p[t], 4);
       mbar_init(&bar_o[t], 1);
       mbar_init(&bar_turn[t], 1);
     }
@@ -248,7 +280,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       __syncwarp();
       if (nt > 0) {
         tc_fence_after();
-        issue_s<D, BF16>(tmem, sq_addr, skv_addr, t, 0);
+        issue_s<D, BF16>(tmem + t * 128, sq_addr + t * C::TILE, skv_addr);
       }
       if (elect_one()) {
         mbar_arrive(&bar_turn[1 - t]);
@@ -267,8 +299,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         mbar_wait(&bar_turn[t], (t == 0 ? j : j + 1) & 1, p.err, 12);
         __syncwarp();
         tc_fence_after();
-        if (pv) issue_pv<D, BF16>(tmem, skv_addr, t, fv % C::NSTAGE, j > 0);
-        if (sn) issue_s<D, BF16>(tmem, sq_addr, skv_addr, t, fk % C::NSTAGE);
+        if (pv) issue_pv<D, BF16>(tmem + 256 + t * 128, tmem + t * 128, skv_addr + (fv % C::NSTAGE) * C::TILE, j > 0);
+        if (sn) issue_s<D, BF16>(tmem + t * 128, sq_addr + t * C::TILE, skv_addr + (fk % C::NSTAGE) * C::TILE);
         if (elect_one()) {
           mbar_arrive(&bar_turn[1 - t]);
           if (pv && !sn) umma_commit(&bar_o[t]);   // last PV of this tile
@@ -425,40 +457,387 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&bar_p[t]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_p[t]);
     }
 
     if (n > 0) {
       mbar_wait(&bar_o[t], 0, p.err, 10);   // committed once, after the last PV
       tc_fence_after();
-      const float inv_l = 1.f / l;
-      const bool valid = qrow < p.Nq;
-      uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
-                      2 * (static_cast<int64_t>(b) * p.o_sb + static_cast<int64_t>(h) * p.o_sh +
-                           static_cast<int64_t>(qrow) * p.o_ss);
+      store_o_lse<D, BF16>(p, tO, b, h, qrow, m, l);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Forward with P in TMEM columns of its own (d <= 96)
+// ---------------------------------------------------------------------------
+// Tensor memory: S_0 [0, 128), S_1 [128, 256), O_0 [256, 256 + D),
+// O_1 [256 + D, 256 + 2 D), and one 64-column P buffer after them that the two
+// query tiles take turns on.  Because P no longer overwrites S, a softmax
+// warp releases S_t,j as soon as it holds it in registers and S_t,j+1 is
+// computed while it works; the tensor cores then wait on a tile's softmax
+// only through its PV.
+//   warps 0-7   softmax / correction / epilogue (tile t = warp / 4, one row
+//               per thread), 224 registers each
+//   warp  8     TMA producer: Q tiles, then K_j (even ring slots) and V_j
+//               (odd ring slots)
+//   warp  9     issuer A: S_t,j = Q_t K_j^T (also allocates TMEM)
+//   warp  10    issuer B: O_t += P V_j
+//   warp  11    idle (completes the third warpgroup for the register split)
+// Writes to the P buffer go in the order (j, t): P_0,0, P_1,0, P_0,1, ...
+// (tiles without key tile j skipped); issuer B issues the PVs in the same
+// order.  A write waits for the PV of the write before it, through that
+// tile's PV barrier at that tile's step: then the buffer is free and, since
+// one issuer's MMAs complete in order, the writer's own PV_t,j-1 is done and
+// O_t may be rescaled.  Per-tile barriers keep every parity wait at most one
+// phase behind its barrier (a single barrier counting all PVs could be two
+// phases behind a softmax warp that ran ahead).
+// P gets TMEM columns of its own when S_0, S_1, O_0, O_1 and a 64-column P
+// buffer fit in 512 columns (d <= 96).
+template <int D>
+constexpr bool kSepP = 256 + 2 * D + 64 <= 512;
+
+template <int D>
+struct FwdSpCfg {
+  using G = TileGeo<D>;
+  static constexpr int TILE = G::TILE;
+  static constexpr int NSTAGE = D == 64 ? 8 : 6;   // even: K_j in even slots, V_j in odd
+  static constexpr int SMEM_DATA = kNQT * TILE + NSTAGE * TILE;
+  static constexpr int NBARS = kNQT + 2 * NSTAGE + 4 * kNQT + 2;
+  static constexpr int SMEM = 1024 + SMEM_DATA + NBARS * 8 + 16;
+  static constexpr int THREADS = 384;
+  static constexpr int PROD_WARP = 8;
+  static constexpr int MMA_WARP = 9;            // issuer A; issuer B is warp 10
+  static constexpr uint32_t kColO = 256;        // O_t at kColO + t * D
+  static constexpr uint32_t kColP = 256 + 2 * D;
+  // Register split: 384 threads launch with 168 registers each (64,512 in
+  // all); the softmax warpgroups take 224, the third warpgroup keeps 56:
+  // 2 * 128 * 224 + 128 * 56 = 64,512.
+  static constexpr uint32_t kRegSoftmax = 224;
+  static constexpr uint32_t kRegOther = 56;
+  static_assert(NSTAGE % 2 == 0, "K and V alternate between even and odd slots");
+  static_assert(kColP + 64 <= 512, "TMEM budget");
+  static_assert(2 * 128 * kRegSoftmax + 128 * kRegOther <= THREADS * 168, "register split exceeds the launch");
+  static_assert(SMEM <= 227 * 1024, "shared memory budget");
+};
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(FwdSpCfg<D>::THREADS, 1)
+    fwd_sp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  using C = FwdSpCfg<D>;
+  constexpr int NS = C::NSTAGE;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sKV = smem + kNQT * C::TILE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + NS * C::TILE);
+  uint64_t* bar_q = bars;                      // [kNQT] Q_t landed
+  uint64_t* bar_full = bar_q + kNQT;           // [NS]
+  uint64_t* bar_empty = bar_full + NS;         // [NS] one release by the issuer that read the slot
+  uint64_t* bar_s = bar_empty + NS;            // [kNQT] S_t,j complete
+  uint64_t* bar_sfree = bar_s + kNQT;          // [kNQT] S_t,j in registers (one arrival per warp)
+  uint64_t* bar_o = bar_sfree + kNQT;          // [kNQT] last PV of tile t complete
+  uint64_t* bar_pv = bar_o + kNQT;             // [kNQT] PV_t,j complete (phase j)
+  uint64_t* bar_pready = bar_pv + kNQT;        // next P write done (one arrival per warp of the writer)
+  uint64_t* bar_drain = bar_pready + 1;        // every MMA of both issuers complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_drain + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const int BH = p.B * p.H;
+  int rank, bh;
+  chunked_order(static_cast<int>(blockIdx.x), p.n_pairs, BH, &rank, &bh);
+  const int pair = p.n_pairs - 1 - rank;
+  const int b = bh / p.H;
+  const int h = bh % p.H;
+  const int q0 = pair * (kNQT * kBM);
+
+  int nkt[kNQT];
+  int n_max = 0;
 #pragma unroll
-      for (int c = 0; c < D / 16; ++c) {
-        uint32_t o[16];
-        tmem_ld16(tO + c * 16, o);
-        tmem_wait_ld();
-        uint4 w0, w1;
-        w0.x = pack2<BF16>(__uint_as_float(o[0]) * inv_l, __uint_as_float(o[1]) * inv_l);
-        w0.y = pack2<BF16>(__uint_as_float(o[2]) * inv_l, __uint_as_float(o[3]) * inv_l);
-        w0.z = pack2<BF16>(__uint_as_float(o[4]) * inv_l, __uint_as_float(o[5]) * inv_l);
-        w0.w = pack2<BF16>(__uint_as_float(o[6]) * inv_l, __uint_as_float(o[7]) * inv_l);
-        w1.x = pack2<BF16>(__uint_as_float(o[8]) * inv_l, __uint_as_float(o[9]) * inv_l);
-        w1.y = pack2<BF16>(__uint_as_float(o[10]) * inv_l, __uint_as_float(o[11]) * inv_l);
-        w1.z = pack2<BF16>(__uint_as_float(o[12]) * inv_l, __uint_as_float(o[13]) * inv_l);
-        w1.w = pack2<BF16>(__uint_as_float(o[14]) * inv_l, __uint_as_float(o[15]) * inv_l);
-        if (valid) {
-          reinterpret_cast<uint4*>(orow + c * 32)[0] = w0;
-          reinterpret_cast<uint4*>(orow + c * 32)[1] = w1;
+  for (int t = 0; t < kNQT; ++t) {
+    nkt[t] = key_tiles(q0 + t * kBM, p.Nq, p.Nk, p.causal);
+    n_max = max(n_max, nkt[t]);
+  }
+
+  if (threadIdx.x == 0) {
+    for (int t = 0; t < kNQT; ++t) {
+      mbar_init(&bar_q[t], 1);
+      mbar_init(&bar_s[t], 1);
+      mbar_init(&bar_sfree[t], 4);
+      mbar_init(&bar_o[t], 1);
+      mbar_init(&bar_pv[t], 1);
+    }
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
+    mbar_init(bar_pready, 4);
+    mbar_init(bar_drain, 2);
+    fence_mbar_init();
+  }
+  if (warp == C::MMA_WARP) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp >= C::PROD_WARP) {
+   setmaxnreg_dec<C::kRegOther>();
+   if (warp == C::PROD_WARP && lane == 0) {
+      // ---------------------------------------------------------------- TMA
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+#pragma unroll
+      for (int t = 0; t < kNQT; ++t) {
+        if (nkt[t] == 0) continue;
+        mbar_arrive_expect_tx(&bar_q[t], C::TILE);
+        for (int c = 0; c < C::G::NCH; ++c)
+          tma_load_4d(sQ + t * C::TILE + c * C::G::CHB, &tmQ, &bar_q[t], c * C::G::CC, q0 + t * kBM, h, b);
+      }
+      // Fill f = 2 j holds K_j, f = 2 j + 1 holds V_j.  A slot is refilled
+      // only after its previous fill has landed, so each slot has at most one
+      // copy in flight; a give-up stops the fills and only the fills issued
+      // are drained.
+      int nfill = 2 * n_max;
+      for (int f = 0; f < nfill; ++f) {
+        const int s = f % NS;
+        const int use = f / NS;
+        if (use > 0 && (!mbar_wait(&bar_empty[s], (use - 1) & 1, p.err, 1) ||
+                        !mbar_wait_drain(&bar_full[s], (use - 1) & 1))) {
+          nfill = f;
+          break;
+        }
+        mbar_arrive_expect_tx(&bar_full[s], C::TILE);
+        const CUtensorMap* map = (f & 1) ? &tmV : &tmK;
+        for (int c = 0; c < C::G::NCH; ++c)
+          tma_load_4d(sKV + s * C::TILE + c * C::G::CHB, map, &bar_full[s], c * C::G::CC, (f >> 1) * kBN, h, b);
+      }
+      for (int f = max(0, nfill - NS); f < nfill; ++f) mbar_wait_drain(&bar_full[f % NS], (f / NS) & 1);
+#pragma unroll
+      for (int t = 0; t < kNQT; ++t)
+        if (nkt[t] > 0) mbar_wait_drain(&bar_q[t], 0);
+   } else if (warp == C::MMA_WARP) {
+    // ------------------------------------------------------ issuer A: S MMAs
+    const uint32_t sq_addr = smem_u32(sQ);
+    const uint32_t skv_addr = smem_u32(sKV);
+    for (int j = 0; j < n_max; ++j) {
+      const int f = 2 * j;
+      mbar_wait(&bar_full[f % NS], (f / NS) & 1, p.err, 3);
+#pragma unroll
+      for (int t = 0; t < kNQT; ++t) {
+        if (j >= nkt[t]) continue;
+        if (j == 0) {
+          mbar_wait(&bar_q[t], 0, p.err, 2);
+        } else {
+          mbar_wait(&bar_sfree[t], (j - 1) & 1, p.err, 13);   // S_t,j-1 read
+        }
+        __syncwarp();
+        tc_fence_after();
+        issue_s<D, BF16>(tmem + t * 128, sq_addr + t * C::TILE, skv_addr + (f % NS) * C::TILE);
+        if (elect_one()) umma_commit(&bar_s[t]);
+      }
+      if (elect_one()) umma_commit(&bar_empty[f % NS]);   // K_j read by every S of step j
+    }
+    if (elect_one()) umma_commit(bar_drain);
+    __syncwarp();
+    mbar_wait_drain(bar_drain, 0);
+   } else if (warp == C::MMA_WARP + 1) {
+    // ----------------------------------------------------- issuer B: PV MMAs
+    const uint32_t skv_addr = smem_u32(sKV);
+    int k = 0;   // number of the next P write
+    for (int j = 0; j < n_max; ++j) {
+      const int f = 2 * j + 1;
+      mbar_wait(&bar_full[f % NS], (f / NS) & 1, p.err, 4);
+#pragma unroll
+      for (int t = 0; t < kNQT; ++t) {
+        if (j >= nkt[t]) continue;
+        mbar_wait(bar_pready, k & 1, p.err, 5);
+        __syncwarp();
+        tc_fence_after();
+        issue_pv<D, BF16>(tmem + C::kColO + t * D, tmem + C::kColP, skv_addr + (f % NS) * C::TILE, j > 0);
+        if (elect_one()) {
+          umma_commit(&bar_pv[t]);
+          if (j == nkt[t] - 1) umma_commit(&bar_o[t]);
+        }
+        ++k;
+      }
+      if (elect_one()) umma_commit(&bar_empty[f % NS]);   // V_j read by every PV of step j
+    }
+    if (elect_one()) umma_commit(bar_drain);
+    __syncwarp();
+    mbar_wait_drain(bar_drain, 0);
+   }
+  } else {
+    setmaxnreg_inc<C::kRegSoftmax>();
+    // ------------------------------------------------- softmax / epilogue
+    const int t = warp >> 2;
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const int r0 = q0 + t * kBM;
+    const int qrow = r0 + row;
+    const int n = nkt[t];
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t tS = tmem + lane_off + t * 128;
+    const uint32_t tO = tmem + lane_off + C::kColO + t * D;
+    const uint32_t tP = tmem + lane_off + C::kColP;
+    const float cs = p.scale_log2;
+    const uint64_t cs2 = f2pack(cs, cs);
+
+    float m = -CUDART_INF_F;  // running max of the scaled scores (log2 domain)
+    float l = 0.f;            // running sum of exp2(score - m)
+
+    for (int j = 0; j < n; ++j) {
+      mbar_wait(&bar_s[t], j & 1, p.err, 8);
+      tc_fence_after();
+      float s[kBN];
+      {
+        uint32_t r0_[32], r1_[32], r2_[32], r3_[32];
+        tmem_ld32(tS, r0_);
+        tmem_ld32(tS + 32, r1_);
+        tmem_ld32(tS + 64, r2_);
+        tmem_ld32(tS + 96, r3_);
+        tmem_wait_ld(r3_);
+        tmem_reg_tie(r0_);
+        tmem_reg_tie(r1_);
+        tmem_reg_tie(r2_);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          s[e] = __uint_as_float(r0_[e]);
+          s[32 + e] = __uint_as_float(r1_[e]);
+          s[64 + e] = __uint_as_float(r2_[e]);
+          s[96 + e] = __uint_as_float(r3_[e]);
         }
       }
-      if (valid) {
-        // LSE = ln(sum_j exp(sm_scale q.k_j)) = ln2 * (m + log2 l)
-        p.lse[(static_cast<int64_t>(b) * p.H + h) * p.Nq + qrow] = (m + log2f(l)) * 0.69314718055994531f;
+      // S_t,j is in registers: the tensor cores may overwrite it with S_t,j+1.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_sfree[t]);
+
+      const int kbase = j * kBN;
+      if (kbase + kBN > p.Nk || (p.causal && kbase + kBN - 1 > r0)) {
+        const int lim = p.causal ? min(p.Nk, qrow + 1) : p.Nk;  // keys < lim are visible
+#pragma unroll
+        for (int c = 0; c < kBN; ++c)
+          if (kbase + c >= lim) s[c] = -CUDART_INF_F;
       }
+      // The write before this one: (tile pt, step pj), or none.
+      int pt = -1, pj = 0;
+      if (t == 1 && j < nkt[0]) {
+        pt = 0;
+        pj = j;
+      } else if (j > 0) {
+        pt = (t == 0 && j - 1 < nkt[1]) ? 1 : t;
+        pj = j - 1;
+      }
+
+      uint32_t pk[kBN / 2];
+      bool done = false;
+      if (j > 0) {
+        // Common case: p = exp2(c s - m) against the running max m.  A row
+        // sum <= 2^8 bounds every p of the row by 2^8, i.e. its max grew by
+        // at most 8 and the exact path below would keep m: this P is its
+        // result.
+        const uint64_t nm2 = f2pack(-m, -m);
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+        for (int e = 0; e < kBN / 2; ++e) {
+          float x0, x1;
+          f2unpack(ffma2(f2pack(s[2 * e], s[2 * e + 1]), cs2, nm2), x0, x1);
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
+          acc[e & 3] = fadd2(acc[e & 3], f2pack(p0, p1));
+          pk[e] = pack2<BF16>(p0, p1);
+        }
+        float a0, a1;
+        f2unpack(fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3])), a0, a1);
+        const float sum = a0 + a1;
+        if (!__any_sync(0xffffffffu, !(sum <= kFastSumBound))) {
+          l += sum;
+          done = true;
+        }
+      }
+      if (pt >= 0) mbar_wait(&bar_pv[pt], pj & 1, p.err, 9);
+      tc_fence_after();
+      if (!done) {
+        // First tile, or a row of this warp may have grown by more than 2^8:
+        // tile max, O_t and l rescaled if the max grew by more than 2^8, p.
+        float mc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mc[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+        for (int c = 16; c < kBN; c += 16) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mc[i] = fmax3(mc[i], s[c + 2 * i], s[c + 2 * i + 1]);
+        }
+        const float mx = fmax3(fmax3(mc[0], mc[1], mc[2]), fmax3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
+        const float m_tile = mx * cs;
+        if (j == 0) {
+          m = m_tile;
+        } else {
+          const bool need = m_tile > m + kRescaleLog2;
+          const float m_new = need ? m_tile : m;
+          const float alpha = ex2_approx(m - m_new);
+          m = m_new;
+          l *= alpha;
+          const uint64_t a2 = f2pack(alpha, alpha);
+#pragma unroll
+          for (int c = 0; c < D / 16; ++c) {
+            uint32_t o[16];
+            tmem_ld16(tO + c * 16, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+              float lo, hi;
+              f2unpack(fmul2(f2pack(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2), lo, hi);
+              o[e] = __float_as_uint(lo);
+              o[e + 1] = __float_as_uint(hi);
+            }
+            tmem_st16(tO + c * 16, o);
+          }
+        }
+        const float mb = (m == -CUDART_INF_F) ? 0.f : m;
+        const uint64_t nm2 = f2pack(-mb, -mb);
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+        for (int e = 0; e < kBN / 2; ++e) {
+          float x0, x1;
+          f2unpack(ffma2(f2pack(s[2 * e], s[2 * e + 1]), cs2, nm2), x0, x1);
+          const float p0 = ex2_approx(x0);
+          const float p1 = ex2_approx(x1);
+          acc[e & 3] = fadd2(acc[e & 3], f2pack(p0, p1));
+          pk[e] = pack2<BF16>(p0, p1);
+        }
+        float a0, a1;
+        f2unpack(fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3])), a0, a1);
+        l += a0 + a1;
+      }
+#pragma unroll
+      for (int i = 0; i < kBN / 32; ++i) tmem_st16(tP + i * 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[i * 16]));
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_pready);
+    }
+
+    if (n > 0) {
+      mbar_wait(&bar_o[t], 0, p.err, 10);
+      tc_fence_after();
+      store_o_lse<D, BF16>(p, tO, b, h, qrow, m, l);
     }
   }
 
@@ -491,12 +870,28 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   p.o_ss = a.o.ss;
   p.lse = a.lse;
   p.err = a.err;
-  auto kern = fwd_kernel<D, BF16>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-  if (e != cudaSuccess) return e;
   const long long blocks = static_cast<long long>(p.n_pairs) * a.B * a.H;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-  kern<<<static_cast<unsigned>(blocks), C::THREADS, C::SMEM, stream>>>(tq, tk, tv, p);
+  if constexpr (kSepP<D>) {
+    using CS = FwdSpCfg<D>;
+    auto kern = fwd_sp_kernel<D, BF16>;
+    // setmaxnreg.inc waits until the block's launch registers cover the
+    // split: never launch a build whose register count would not.
+    static const int num_regs = [&] {
+      cudaFuncAttributes fattr{};
+      return cudaFuncGetAttributes(&fattr, kern) == cudaSuccess ? fattr.numRegs : 0;
+    }();
+    if (num_regs * CS::THREADS < 2 * 128 * static_cast<int>(CS::kRegSoftmax) + 128 * static_cast<int>(CS::kRegOther))
+      return cudaErrorInvalidConfiguration;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CS::SMEM);
+    if (e != cudaSuccess) return e;
+    kern<<<static_cast<unsigned>(blocks), CS::THREADS, CS::SMEM, stream>>>(tq, tk, tv, p);
+  } else {
+    auto kern = fwd_kernel<D, BF16>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    kern<<<static_cast<unsigned>(blocks), C::THREADS, C::SMEM, stream>>>(tq, tk, tv, p);
+  }
   return cudaGetLastError();
 }
 
