@@ -763,6 +763,10 @@ __global__ void __launch_bounds__(FwdSpCfg<D>::THREADS, 1)
           acc[e & 3] = fadd2(acc[e & 3], f2pack(p0, p1));
           pk[e] = pack2<BF16>(p0, p1);
         }
+        // P complete before the wait for the buffer: the compiler may
+        // otherwise sink its conversions past the wait.
+        tmem_reg_tie(*reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+        tmem_reg_tie(*reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
         float a0, a1;
         f2unpack(fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3])), a0, a1);
         const float sum = a0 + a1;
