@@ -48,6 +48,9 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--fwd-only", action="store_true",
+                    help="time only the forward of --workload (the forward-only configurations), one JSON line")
+    ap.add_argument("--split", default="1", help="with --fwd-only: key-range splits (an integer, or 'auto')")
     ap.add_argument("--source-hash", default=None, metavar="KERNEL",
                     help="print the source hash that a traffic line for KERNEL must carry, and exit")
     return ap.parse_args(argv)
@@ -319,6 +322,91 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
 
 
+def run_fwd_only(args):
+    """Forward alone on one of the forward-only workloads, optionally split
+    over key ranges (fa_fwd_split).  Inputs smaller than L2 are made cold by
+    writing a 256 MB scratch buffer between steps, outside the timed kernels;
+    each step is timed with CUDA events around the forward launches only."""
+    import torch
+
+    from tiled_attention_07_gb300 import fa
+    from tiled_attention_07_gb300 import workloads as W
+
+    rank, world = dist_init("nccl")
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = pick_workload(args)
+    x = {k: t.to(dev) for k, t in W.make_inputs(w, device="cpu", with_grad_output=False).items()}
+    q, k, v = x["q"], x["k"], x["v"]
+    o = torch.empty_like(q)
+    lse = torch.empty(fa.lse_shape(q), dtype=torch.float32, device=dev)
+    B, H, Nq, d = fa._dims(q)
+    Nk = fa._dims(k)[2]
+    n_splits = fa.fa_fwd_split_count(B, H, Nq, Nk, d, w.causal) if args.split == "auto" else int(args.split)
+    nbytes = fa.fa_fwd_split_workspace_bytes(B, H, Nq, d, n_splits)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    in_bytes = sum(t.numel() * t.element_size() for t in (q, k, v))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if in_bytes < (256 << 20) else None
+
+    def fwd():
+        if n_splits > 1:
+            fa.fa_fwd_split(q, k, v, o, lse, w.sm_scale, w.causal, n_splits, ws, stream)
+        else:
+            fa.fa_fwd(q, k, v, o, lse, w.sm_scale, w.causal, stream)
+
+    for _ in range(max(args.warmup, 3)):
+        fwd()
+    torch.cuda.synchronize(dev)
+    rc, detail = fa.fa_last_device_error(stream)
+    if rc != fa.FA_OK:
+        raise RuntimeError(f"device error after warm-up: {detail:#x}")
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    clocks = ClockSampler() if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize(dev)
+    for i in range(K):
+        if flush is not None:
+            flush.fill_(i & 255)
+        evs[i][0].record(stream)
+        fwd()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clk = clocks.stop() if clocks else None
+    rc, detail = fa.fa_last_device_error(stream)
+    if rc != fa.FA_OK:
+        raise RuntimeError(f"device error in the timed region: {detail:#x}")
+    ms = reduce_max(sum(a.elapsed_time(b) for a, b in evs), dev)
+    ms_step = ms / K
+    flops = w.fwd_flops()
+    value = world * flops / (ms_step / 1e3) / 1e12
+    peaks, peak_src = load_peaks()
+    peak = peaks["bf16_tflops"]
+    line = {
+        "metric": "attention forward TFLOP/s on 1 GB300 (forward-only configuration)", "value": round(value, 2),
+        "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": max(args.warmup, 3),
+        "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic (seeded q, k, v)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": w.causal,
+                   "layout": w.layout, "split": n_splits, "flops_per_step": flops,
+                   "l2": "256 MB scratch write between steps" if flush is not None else "inputs larger than L2",
+                   "parallelism": f"replica x{world}"},
+        "roofline": {"bound": "tensor", "kernel": "fwd" + ("+merge" if n_splits > 1 else ""),
+                     "achieved": round(value / world, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(value / world / peak, 4), "traffic": None,
+                     "peak_source": f"{peak_src} bf16 burst (kernel timed alone)"},
+        "clocks": clk, "gpu_launches": K * (2 if n_splits > 1 else 1), "e2e": None, "cpu_baseline": None,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_e2e(args, w, host, dev, stream, world):
     """Same metric through the public API with host buffers: every step copies
     q, k, v, dO from pinned host memory, runs forward and backward, and copies
@@ -454,6 +542,8 @@ def main(argv=None):
         return
     if args.impl == "reference":
         run_reference(args)
+    elif args.fwd_only:
+        run_fwd_only(args)
     else:
         run_ours(args)
     import torch.distributed as dist

@@ -105,6 +105,51 @@ FA_API fa_status fa_fwd_strided(const void* q, const void* k, const void* v, voi
                          fa_dtype dtype, const fa_layout* layout, void* stream);
 
 /*
+ * Split-KV forward: the key tiles of every query tile are divided into
+ * n_splits contiguous ranges handled by different CTAs, so that problems with
+ * few query tiles still fill the GPU.  Split s covers key tiles
+ * [s*T, min((s+1)*T, nk)) with nk = ceil(Nk/128), T = ceil(nk/n_splits).
+ * Each split writes, per query row, its own softmax over its keys: O_s (the
+ * partial output already divided by its own row sum) and lse_s (its own
+ * log-sum-exp; -inf and O_s = 0 when the row sees none of its keys).  A merge
+ * kernel then combines them with the rescaling of the online softmax
+ * ("[CS336]", "FlashAttention V2 / Forward Pass": m' = max, l' = e^(m-m') l
+ * + ...; "Puzzles 8 Long Softmax": sum' = sum * exp(m1 - m2) + ...):
+ *     lse = log sum_s exp(lse_s),   O = sum_s exp(lse_s - lse) O_s,
+ * which equals the one-pass result up to rounding.
+ *
+ * fa_fwd_split_workspace_bytes -- scratch for the partial results: float32
+ * O_s and lse_s of every split, query rows padded to whole 128-row tiles:
+ * 4 * n_splits * B*H*ceil(Nq/128)*128 * (d + 1) bytes.  0 for n_splits < 2.
+ */
+FA_API size_t fa_fwd_split_workspace_bytes(int B, int H, int Nq, int d, int n_splits);
+
+/*
+ * fa_fwd_split_count -- a split count for this problem on the current device:
+ * the most splits for which the split grid still fits in one wave (one CTA
+ * per SM) while every split keeps at least 4 of the 128-key tiles, capped at
+ * FA_MAX_SPLITS; 1 when the unsplit grid already fills the SMs.  (Each CTA
+ * has a fixed start-up and drain cost of a few key tiles' work, so more
+ * splits than that are slower.)  Returns 1 for invalid or empty problems.
+ */
+#define FA_MAX_SPLITS 64
+FA_API int fa_fwd_split_count(int B, int H, int Nq, int Nk, int d, int causal);
+
+/*
+ * fa_fwd_split -- fa_fwd / fa_fwd_strided over n_splits key ranges (1 <=
+ * n_splits <= FA_MAX_SPLITS).  layout: strides of q, k, v, o, or NULL for
+ * contiguous [B, H, seq, d].  n_splits == 1 runs the one-pass forward and
+ * needs no workspace; otherwise workspace (device, 16-byte aligned, owned by
+ * the caller, contents on entry ignored) must hold
+ * fa_fwd_split_workspace_bytes(B, H, Nq, d, n_splits) bytes, else
+ * FA_ERR_WORKSPACE.  Two launches on `stream` (partial forward, merge).
+ */
+FA_API fa_status fa_fwd_split(const void* q, const void* k, const void* v, void* o, float* lse,
+                       int B, int H, int Nq, int Nk, int d, float sm_scale, int causal,
+                       fa_dtype dtype, const fa_layout* layout, int n_splits, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/*
  * fa_bwd_workspace_bytes -- size of the scratch buffer fa_bwd needs: the
  * per-row D = rowsum(O o dO) and the log2-domain LSE, float32, padded to
  * whole 128-row query tiles: 2 * 4 * B*H*ceil(Nq/128)*128 bytes.

@@ -44,6 +44,8 @@ __all__ = [
     "probabilities",
     "forward",
     "backward",
+    "forward_keys",
+    "merge",
     "forward_heads",
     "backward_heads",
 ]
@@ -97,6 +99,54 @@ def forward(q, k, v, sm_scale: float, causal: bool):
     """
     p, lse = probabilities(q, k, sm_scale, causal)
     o = p @ _as64(v)
+    return o, lse
+
+
+def forward_keys(q, k, v, sm_scale: float, causal: bool, k_begin: int, k_end: int):
+    """The softmax of each query row over the keys [k_begin, k_end) only.
+
+    Key indices are absolute (the causal mask still keeps key j for query i
+    iff j <= i).  Returns ``(O_s [Nq, d], lse_s [Nq])``: O_s is P_s V with P_s
+    the row softmax restricted to the range, lse_s the natural log of
+    sum_{j in range} exp(S_ij).  A row that sees no key of the range has
+    lse_s = -inf and O_s = 0 (an empty sum).
+    """
+    s = scores(q, k, sm_scale, causal)[:, k_begin:k_end]
+    v = _as64(v)[k_begin:k_end]
+    nq = s.shape[0]
+    o = np.zeros((nq, v.shape[1]))
+    lse = np.full(nq, -np.inf)
+    for i in range(nq):
+        row = s[i]
+        if row.size == 0 or not np.isfinite(row).any():
+            continue
+        m = np.max(row)
+        e = np.exp(row - m)
+        z = np.sum(e)
+        lse[i] = m + np.log(z)
+        o[i] = (e / z) @ v
+    return o, lse
+
+
+def merge(o_parts, lse_parts):
+    """Combine per-key-range softmax results into the softmax over their union.
+
+    The rescaling step of the online softmax ("[CS336] Assignment 2:
+    Systems", "FlashAttention V2 / Forward Pass": a new running max m' and
+    l' = e^(m - m') l + ...; "Puzzles 8 Long Softmax": sum' = sum * exp(m1 -
+    m2) + ...) applied to whole ranges: lse = log sum_s exp(lse_s) and
+    O = sum_s exp(lse_s - lse) O_s.  ``o_parts`` is [S, Nq, d], ``lse_parts``
+    [S, Nq]; ranges that a row does not see carry lse_s = -inf.
+    """
+    o_parts = np.asarray(o_parts, dtype=np.float64)
+    lse_parts = np.asarray(lse_parts, dtype=np.float64)
+    m = np.max(lse_parts, axis=0)
+    seen = np.isfinite(m)
+    ms = np.where(seen, m, 0.0)
+    w = np.exp(lse_parts - ms[None, :])                  # [S, Nq]; 0 for unseen ranges
+    z = np.sum(w, axis=0)
+    lse = np.where(seen, ms + np.log(np.where(seen, z, 1.0)), -np.inf)
+    o = np.einsum("sn,snd->nd", w, o_parts) / np.where(seen, z, 1.0)[:, None]
     return o, lse
 
 

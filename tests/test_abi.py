@@ -7,6 +7,7 @@ import os
 import re
 
 import pytest
+import torch
 
 from tiled_attention_07_gb300 import fa
 
@@ -130,3 +131,48 @@ def test_binding_refuses_cpu_tensors():
     q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         fa.attention_forward(q, q, q, 0.125, False)
+
+
+def test_split_workspace_bytes(L):
+    # float32 O_s (d columns) and lse_s per split, rows padded to 128-row tiles
+    assert fa.fa_fwd_split_workspace_bytes(1, 16, 1000, 80, 4) == 4 * 4 * 16 * 1024 * 81
+    assert fa.fa_fwd_split_workspace_bytes(4, 12, 512, 64, 2) == 4 * 2 * 48 * 512 * 65
+    assert fa.fa_fwd_split_workspace_bytes(1, 16, 1000, 80, 1) == 0
+    assert fa.fa_fwd_split_workspace_bytes(0, 16, 1000, 80, 4) == 0
+    assert fa.fa_fwd_split_workspace_bytes(1, 16, 0, 80, 4) == 0
+
+
+def test_split_count_without_a_device_is_one(L):
+    if torch.cuda.is_available():
+        pytest.skip("the count depends on the device's SMs")
+    assert fa.fa_fwd_split_count(1, 16, 1000, 2500, 80, False) == 1
+
+
+def split(L, n_splits=4, ws=FAKE, ws_bytes=1 << 30, layout=None, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=1, Nq=128, Nk=1024, d=64, scale=0.125, causal=0,
+             dtype=fa.FA_BF16)
+    a.update(kw)
+    return L.fa_fwd_split(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Nq"], a["Nk"], a["d"],
+                          a["scale"], a["causal"], a["dtype"], layout, n_splits, ws, ws_bytes, None)
+
+
+def test_split_checks_count_workspace_and_args(L):
+    need = fa.fa_fwd_split_workspace_bytes(1, 1, 128, 64, 4)
+    assert split(L, n_splits=0) == fa.FA_ERR_INVALID_ARG
+    assert split(L, n_splits=-3) == fa.FA_ERR_INVALID_ARG
+    assert split(L, n_splits=65) == fa.FA_ERR_INVALID_ARG
+    assert split(L, ws=None) == fa.FA_ERR_WORKSPACE
+    assert split(L, ws_bytes=need - 16) == fa.FA_ERR_WORKSPACE
+    assert split(L, ws=FAKE + 8) == fa.FA_ERR_WORKSPACE
+    assert split(L, d=96) == fa.FA_ERR_UNSUPPORTED
+    assert split(L, Nk=0) == fa.FA_ERR_INVALID_ARG
+    assert split(L, scale=float("nan")) == fa.FA_ERR_INVALID_ARG
+    assert split(L, k=FAKE + 8) == fa.FA_ERR_INVALID_ARG
+    # empty problems are no-ops, with or without a workspace
+    assert split(L, B=0, ws=None) == fa.FA_OK
+    assert split(L, Nq=0, ws=None) == fa.FA_OK
+    lay = fa.Layout()
+    for n in ("q", "k", "v", "o"):
+        setattr(lay, n, fa.Strides(1024 * 64, 1024 * 64, 64))
+    lay.v = fa.Strides(1024 * 64, 1024 * 64, 60)   # 120-byte rows
+    assert split(L, layout=ctypes.byref(lay)) == fa.FA_ERR_INVALID_ARG

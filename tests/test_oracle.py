@@ -224,8 +224,33 @@ def pin_backward_identities(impl):
         np.testing.assert_allclose(dv.sum(axis=0), do.sum(axis=0), atol=1e-12, rtol=0)
 
 
+def pin_split_merge(impl):
+    """Softmaxes over disjoint key ranges, merged, equal the softmax over all keys.
+
+    Checked against the full forward (itself pinned by brute force above):
+    random partitions of the keys, with empty ranges and ranges a causal row
+    sees none of, and the one-range partition."""
+    g = rng(7)
+    for (nq, nk, d, causal, scale) in [(9, 13, 3, False, 0.8), (11, 11, 4, True, 1.2), (6, 15, 2, True, 0.6),
+                                       (14, 5, 3, True, 1.5), (7, 20, 5, False, 2.5)]:
+        q = g.normal(size=(nq, d))
+        k = g.normal(size=(nk, d))
+        v = g.normal(size=(nk, d))
+        o_ref, lse_ref = impl.forward(q, k, v, scale, causal)
+        o1, lse1 = impl.forward_keys(q, k, v, scale, causal, 0, nk)
+        np.testing.assert_allclose(o1, o_ref, atol=1e-13, rtol=0)
+        np.testing.assert_allclose(lse1, lse_ref, atol=1e-13, rtol=0)
+        for trial in range(4):
+            cuts = np.sort(g.integers(0, nk + 1, size=g.integers(1, 5)))
+            bounds = [0] + list(cuts) + [nk]
+            parts = [impl.forward_keys(q, k, v, scale, causal, a, b) for a, b in zip(bounds[:-1], bounds[1:])]
+            o, lse = impl.merge([p[0] for p in parts], [p[1] for p in parts])
+            np.testing.assert_allclose(o, o_ref, atol=1e-13, rtol=0)
+            np.testing.assert_allclose(lse, lse_ref, atol=1e-13, rtol=0)
+
+
 ALL_PINS = [pin_bruteforce, pin_golden, pin_closed_forms, pin_invariants, pin_finite_differences,
-            pin_backward_identities]
+            pin_backward_identities, pin_split_merge]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=[p.__name__ for p in ALL_PINS])
@@ -257,7 +282,7 @@ def test_batched_helpers_match_single_head():
 # planted mistakes: each must be caught by at least one pin
 # ---------------------------------------------------------------------------
 
-def _mutant(scores=None, probabilities=None, forward=None, backward=None):
+def _mutant(scores=None, probabilities=None, forward=None, backward=None, forward_keys=None, merge=None):
     """An implementation object built from the oracle with one piece replaced."""
     m = types.SimpleNamespace()
     m.scores = scores or ref.scores
@@ -285,6 +310,8 @@ def _mutant(scores=None, probabilities=None, forward=None, backward=None):
         return sm_scale * ds @ k, sm_scale * ds.T @ q, dv, dsum
 
     m.backward = backward or _bwd
+    m.forward_keys = forward_keys or ref.forward_keys
+    m.merge = merge or ref.merge
     return m
 
 
@@ -364,6 +391,20 @@ def _bwd_sign_flip(q, k, v, do, sm_scale, causal):
     return -dq, dk, dv, dsum
 
 
+def _merge_equal_weights(o_parts, lse_parts):
+    o_parts = np.asarray(o_parts, float)
+    lse_parts = np.asarray(lse_parts, float)
+    seen = np.isfinite(lse_parts)
+    o = np.sum(np.where(seen[..., None], o_parts, 0.0), axis=0) / np.maximum(seen.sum(axis=0), 1)[:, None]
+    return o, ref.merge(o_parts, lse_parts)[1]
+
+
+def _forward_keys_relative_mask(q, k, v, sm_scale, causal, k_begin, k_end):
+    # causal mask applied with key indices relative to the range
+    return ref.forward_keys(q, np.asarray(k, float)[k_begin:k_end], np.asarray(v, float)[k_begin:k_end],
+                            sm_scale, causal, 0, k_end - k_begin)
+
+
 MUTANTS = {
     "no_scale": _mutant(scores=_scores_no_scale),
     "mask_flipped": _mutant(scores=_scores_mask_flipped),
@@ -375,6 +416,8 @@ MUTANTS = {
     "bwd_dk_wrong_operand": _mutant(backward=_bwd_dk_wrong_operand),
     "bwd_dv_untransposed": _mutant(backward=_bwd_dv_untransposed),
     "bwd_sign_flip": _mutant(backward=_bwd_sign_flip),
+    "merge_equal_weights": _mutant(merge=_merge_equal_weights),
+    "split_relative_mask": _mutant(forward_keys=_forward_keys_relative_mask),
 }
 
 

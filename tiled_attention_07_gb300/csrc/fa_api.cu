@@ -106,13 +106,23 @@ Tensor4 strided(const void* p, const fa_strides& s) {
   return t;
 }
 
+size_t split_ws_bytes(int B, int H, int Nq, int d, int n_splits) {
+  if (n_splits < 2 || B <= 0 || H <= 0 || Nq <= 0 || d <= 0) return 0;
+  return sizeof(float) * static_cast<size_t>(n_splits) * B * H * nq_pad(Nq) * (d + 1);
+}
+
 fa_status fwd_impl(const Tensor4& q, const Tensor4& k, const Tensor4& v, const Tensor4& o, float* lse, int B, int H,
-                   int Nq, int Nk, int d, float sm_scale, int causal, fa_dtype dtype, void* stream) {
+                   int Nq, int Nk, int d, float sm_scale, int causal, fa_dtype dtype, void* stream,
+                   int n_splits = 1, void* workspace = nullptr, size_t workspace_bytes = 0) {
+  if (n_splits < 1 || n_splits > FA_MAX_SPLITS) return FA_ERR_INVALID_ARG;
   fa_status st = check_common(B, H, Nq, Nk, d, sm_scale, causal, dtype);
   if (st != FA_OK) return st;
   if (B == 0 || H == 0 || Nq == 0) return FA_OK;
   if (!valid_tensor(q) || !valid_tensor(k) || !valid_tensor(v) || !valid_tensor(o)) return FA_ERR_INVALID_ARG;
   if (lse == nullptr || !aligned16(lse)) return FA_ERR_INVALID_ARG;
+  if (n_splits > 1 && (workspace == nullptr || !aligned16(workspace) ||
+                       workspace_bytes < split_ws_bytes(B, H, Nq, d, n_splits)))
+    return FA_ERR_WORKSPACE;
   if (get_encode() == nullptr) return FA_ERR_CUDA;
   cudaError_t e;
   int* err = err_word(&e);
@@ -132,6 +142,8 @@ fa_status fwd_impl(const Tensor4& q, const Tensor4& k, const Tensor4& v, const T
   a.causal = causal;
   a.bf16 = dtype == FA_BF16;
   a.err = err;
+  a.n_splits = n_splits;
+  a.part = static_cast<float*>(workspace);
   e = launch_fwd(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -224,6 +236,42 @@ fa_status fa_fwd_strided(const void* q, const void* k, const void* v, void* o, f
   if (layout == nullptr) return FA_ERR_INVALID_ARG;
   return fa::fwd_impl(fa::strided(q, layout->q), fa::strided(k, layout->k), fa::strided(v, layout->v),
                       fa::strided(o, layout->o), lse, B, H, Nq, Nk, d, sm_scale, causal, dtype, stream);
+}
+
+size_t fa_fwd_split_workspace_bytes(int B, int H, int Nq, int d, int n_splits) {
+  return fa::split_ws_bytes(B, H, Nq, d, n_splits);
+}
+
+int fa_fwd_split_count(int B, int H, int Nq, int Nk, int d, int causal) {
+  (void)d;
+  (void)causal;
+  if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0) return 1;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      sms <= 0)
+    return 1;
+  // Every CTA pays a fixed start-up and drain time of a few key tiles' work,
+  // so a split only pays while the split grid still runs in one wave and
+  // every split keeps at least kMinTilesPerSplit key tiles.
+  constexpr long long kMinTilesPerSplit = 4;
+  const long long ctas = static_cast<long long>((Nq + 255) / 256) * B * H;   // two query tiles per CTA
+  const long long n_kt = (Nk + 127) / 128;
+  long long s = sms / ctas;
+  if (s > n_kt / kMinTilesPerSplit) s = n_kt / kMinTilesPerSplit;
+  if (s > FA_MAX_SPLITS) s = FA_MAX_SPLITS;
+  return s < 1 ? 1 : static_cast<int>(s);
+}
+
+fa_status fa_fwd_split(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                       int Nk, int d, float sm_scale, int causal, fa_dtype dtype, const fa_layout* layout,
+                       int n_splits, void* workspace, size_t workspace_bytes, void* stream) {
+  if (layout == nullptr)
+    return fa::fwd_impl(fa::contiguous(q, H, Nq, d), fa::contiguous(k, H, Nk, d), fa::contiguous(v, H, Nk, d),
+                        fa::contiguous(o, H, Nq, d), lse, B, H, Nq, Nk, d, sm_scale, causal, dtype, stream, n_splits,
+                        workspace, workspace_bytes);
+  return fa::fwd_impl(fa::strided(q, layout->q), fa::strided(k, layout->k), fa::strided(v, layout->v),
+                      fa::strided(o, layout->o), lse, B, H, Nq, Nk, d, sm_scale, causal, dtype, stream, n_splits,
+                      workspace, workspace_bytes);
 }
 
 size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int Nk, int d) {

@@ -76,6 +76,13 @@ struct FwdParams {
   int64_t o_sb, o_sh, o_ss;
   float* lse;
   int* err;
+  // Split-KV: block b works on split b % n_splits, key tiles
+  // [split * tiles_per_split, (split + 1) * tiles_per_split).
+  int n_splits;
+  int tiles_per_split;
+  int Nqp;              // query rows padded to whole tiles (partial buffers)
+  float* part_o;        // [n_splits][B*H][Nqp][d]
+  float* part_lse;      // [n_splits][B*H][Nqp]
 };
 
 // Number of key tiles query tile t (rows r0 .. r0+127) needs.
@@ -120,6 +127,36 @@ __device__ __forceinline__ void store_o_lse(const FwdParams& p, uint32_t tO, int
     }
   }
   if (valid) p.lse[(static_cast<int64_t>(b) * p.H + h) * p.Nq + qrow] = (m + log2f(l)) * 0.69314718055994531f;
+}
+
+// Epilogue of one query row in split mode: the split's own softmax output
+// O_s = O_acc / l and lse_s = ln 2 * (m + log2 l) in float32, or O_s = 0 and
+// lse_s = -inf when the row saw no key of the split (have == false).
+template <int D>
+__device__ __forceinline__ void store_partial(const FwdParams& p, uint32_t tO, int bh, int split, int qrow,
+                                              float m, float l, bool have) {
+  const bool valid = qrow < p.Nq;
+  const size_t row = (static_cast<size_t>(split) * p.B * p.H + bh) * p.Nqp + qrow;
+  float4* dst = reinterpret_cast<float4*>(p.part_o + row * D);
+  const float inv_l = have ? 1.f / l : 0.f;
+#pragma unroll
+  for (int c = 0; c < D / 16; ++c) {
+    uint32_t o[16];
+    if (have) {
+      tmem_ld16(tO + c * 16, o);
+      tmem_wait_ld();
+    } else {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) o[e] = 0u;
+    }
+    if (valid) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        dst[c * 4 + i] = make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
+                                     __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
+    }
+  }
+  if (valid) p.part_lse[row] = have ? (m + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
 }
 
 // S = Q_t K_j^T into TMEM columns [d_tmem, d_tmem + 128): M = 128 queries,
@@ -176,18 +213,21 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
   // Work decode: heads in chunks sharing K/V through L2; inside a chunk the
   // heaviest query-tile pairs first (longest-processing-time order for causal).
   const int BH = p.B * p.H;
+  const int split = static_cast<int>(blockIdx.x) % p.n_splits;
   int rank, bh;
-  chunked_order(static_cast<int>(blockIdx.x), p.n_pairs, BH, &rank, &bh);
+  chunked_order(static_cast<int>(blockIdx.x) / p.n_splits, p.n_pairs, BH, &rank, &bh);
   const int pair = p.n_pairs - 1 - rank;
   const int b = bh / p.H;
   const int h = bh % p.H;
   const int q0 = pair * (kNQT * kBM);
+  const int kt0 = split * p.tiles_per_split;   // first key tile of this block
 
+  // Key tiles of query tile t in this block: [kt0, kt0 + nkt[t]).
   int nkt[kNQT];
   int n_max = 0;
 #pragma unroll
   for (int t = 0; t < kNQT; ++t) {
-    nkt[t] = key_tiles(q0 + t * kBM, p.Nq, p.Nk, p.causal);
+    nkt[t] = max(0, min(key_tiles(q0 + t * kBM, p.Nq, p.Nk, p.causal), kt0 + p.tiles_per_split) - kt0);
     n_max = max(n_max, nkt[t]);
   }
 
@@ -243,7 +283,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           break;
         }
         mbar_arrive_expect_tx(&bar_full[s], C::TILE);
-        const int j = f >> 1;
+        const int j = kt0 + (f >> 1);
         const CUtensorMap* map = (f & 1) ? &tmV : &tmK;
         for (int c = 0; c < C::G::NCH; ++c)
           tma_load_4d(sKV + s * C::TILE + c * C::G::CHB, map, &bar_full[s], c * C::G::CC, j * kBN, h, b);
@@ -321,7 +361,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     const int row = quad * 32 + lane;
     const int r0 = q0 + t * kBM;
     const int qrow = r0 + row;
-    const int n = key_tiles(r0, p.Nq, p.Nk, p.causal);
+    const int n = nkt[t];
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t tS = tmem + lane_off + t * 128;
     const uint32_t tO = tmem + lane_off + 256 + t * 128;
@@ -346,7 +386,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       }
       tmem_wait_ld();
 
-      const int kbase = j * kBN;
+      const int kbase = (kt0 + j) * kBN;
       const bool tail = kbase + kBN > p.Nk;
       const bool diag = p.causal && (kbase + kBN - 1 > r0);
       if (tail || diag) {
@@ -461,7 +501,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       if (lane == 0) mbar_arrive(&bar_p[t]);
     }
 
-    if (n > 0) {
+    if (p.n_splits > 1) {
+      if (n > 0) {
+        mbar_wait(&bar_o[t], 0, p.err, 10);
+        tc_fence_after();
+      }
+      store_partial<D>(p, tO, bh, split, qrow, m, l, n > 0);
+    } else if (n > 0) {
       mbar_wait(&bar_o[t], 0, p.err, 10);   // committed once, after the last PV
       tc_fence_after();
       store_o_lse<D, BF16>(p, tO, b, h, qrow, m, l);
@@ -555,18 +601,21 @@ __global__ void __launch_bounds__(FwdSpCfg<D>::THREADS, 1)
   const int lane = threadIdx.x & 31;
 
   const int BH = p.B * p.H;
+  const int split = static_cast<int>(blockIdx.x) % p.n_splits;
   int rank, bh;
-  chunked_order(static_cast<int>(blockIdx.x), p.n_pairs, BH, &rank, &bh);
+  chunked_order(static_cast<int>(blockIdx.x) / p.n_splits, p.n_pairs, BH, &rank, &bh);
   const int pair = p.n_pairs - 1 - rank;
   const int b = bh / p.H;
   const int h = bh % p.H;
   const int q0 = pair * (kNQT * kBM);
+  const int kt0 = split * p.tiles_per_split;   // first key tile of this block
 
+  // Key tiles of query tile t in this block: [kt0, kt0 + nkt[t]).
   int nkt[kNQT];
   int n_max = 0;
 #pragma unroll
   for (int t = 0; t < kNQT; ++t) {
-    nkt[t] = key_tiles(q0 + t * kBM, p.Nq, p.Nk, p.causal);
+    nkt[t] = max(0, min(key_tiles(q0 + t * kBM, p.Nq, p.Nk, p.causal), kt0 + p.tiles_per_split) - kt0);
     n_max = max(n_max, nkt[t]);
   }
 
@@ -625,7 +674,8 @@ __global__ void __launch_bounds__(FwdSpCfg<D>::THREADS, 1)
         mbar_arrive_expect_tx(&bar_full[s], C::TILE);
         const CUtensorMap* map = (f & 1) ? &tmV : &tmK;
         for (int c = 0; c < C::G::NCH; ++c)
-          tma_load_4d(sKV + s * C::TILE + c * C::G::CHB, map, &bar_full[s], c * C::G::CC, (f >> 1) * kBN, h, b);
+          tma_load_4d(sKV + s * C::TILE + c * C::G::CHB, map, &bar_full[s], c * C::G::CC, (kt0 + (f >> 1)) * kBN,
+                      h, b);
       }
       for (int f = max(0, nfill - NS); f < nfill; ++f) mbar_wait_drain(&bar_full[f % NS], (f / NS) & 1);
 #pragma unroll
@@ -728,7 +778,7 @@ __global__ void __launch_bounds__(FwdSpCfg<D>::THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_sfree[t]);
 
-      const int kbase = j * kBN;
+      const int kbase = (kt0 + j) * kBN;
       if (kbase + kBN > p.Nk || (p.causal && kbase + kBN - 1 > r0)) {
         const int lim = p.causal ? min(p.Nk, qrow + 1) : p.Nk;  // keys < lim are visible
 #pragma unroll
@@ -838,7 +888,13 @@ __global__ void __launch_bounds__(FwdSpCfg<D>::THREADS, 1)
       if (lane == 0) mbar_arrive(bar_pready);
     }
 
-    if (n > 0) {
+    if (p.n_splits > 1) {
+      if (n > 0) {
+        mbar_wait(&bar_o[t], 0, p.err, 10);
+        tc_fence_after();
+      }
+      store_partial<D>(p, tO, bh, split, qrow, m, l, n > 0);
+    } else if (n > 0) {
       mbar_wait(&bar_o[t], 0, p.err, 10);
       tc_fence_after();
       store_o_lse<D, BF16>(p, tO, b, h, qrow, m, l);
@@ -851,6 +907,64 @@ __global__ void __launch_bounds__(FwdSpCfg<D>::THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+}
+
+// ---------------------------------------------------------------------------
+// Split-KV merge: one warp per query row
+// ---------------------------------------------------------------------------
+// lse = log sum_s exp(lse_s) and O = sum_s exp(lse_s - lse) O_s: the
+// rescaling step of the online softmax applied to whole key ranges.
+struct MergeParams {
+  const float* part_o;
+  const float* part_lse;
+  int n_splits, BH, H, Nq, Nqp;
+  void* o;
+  int64_t o_sb, o_sh, o_ss;
+  float* lse;
+};
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(128) fwd_merge_kernel(const MergeParams mp) {
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const long long r = static_cast<long long>(blockIdx.x) * 4 + warp;
+  if (r >= static_cast<long long>(mp.BH) * mp.Nq) return;
+  const int bh = static_cast<int>(r / mp.Nq);
+  const int q = static_cast<int>(r % mp.Nq);
+  const size_t stride = static_cast<size_t>(mp.BH) * mp.Nqp;   // rows between splits
+  const size_t row0 = static_cast<size_t>(bh) * mp.Nqp + q;
+  float mx = -CUDART_INF_F;
+  for (int s = 0; s < mp.n_splits; ++s) mx = fmaxf(mx, mp.part_lse[row0 + s * stride]);
+  float wsum = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const bool col = lane < D / 4;   // this lane's 4 columns
+  if (mx != -CUDART_INF_F) {
+    for (int s = 0; s < mp.n_splits; ++s) {
+      const size_t row = row0 + s * stride;
+      const float w = expf(mp.part_lse[row] - mx);
+      wsum += w;
+      if (col && w != 0.f) {
+        const float4 v = reinterpret_cast<const float4*>(mp.part_o + row * D)[lane];
+        acc.x += w * v.x;
+        acc.y += w * v.y;
+        acc.z += w * v.z;
+        acc.w += w * v.w;
+      }
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  const int b = bh / mp.H;
+  const int h = bh % mp.H;
+  if (col) {
+    uint8_t* orow = reinterpret_cast<uint8_t*>(mp.o) +
+                    2 * (static_cast<int64_t>(b) * mp.o_sb + static_cast<int64_t>(h) * mp.o_sh +
+                         static_cast<int64_t>(q) * mp.o_ss);
+    uint2 w2;
+    w2.x = pack2<BF16>(acc.x * inv, acc.y * inv);
+    w2.y = pack2<BF16>(acc.z * inv, acc.w * inv);
+    reinterpret_cast<uint2*>(orow)[lane] = w2;
+  }
+  if (lane == 0) mp.lse[static_cast<size_t>(bh) * mp.Nq + q] = wsum > 0.f ? mx + logf(wsum) : -CUDART_INF_F;
 }
 
 template <int D, bool BF16>
@@ -874,7 +988,14 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   p.o_ss = a.o.ss;
   p.lse = a.lse;
   p.err = a.err;
-  const long long blocks = static_cast<long long>(p.n_pairs) * a.B * a.H;
+  const int n_kt = (a.Nk + kBN - 1) / kBN;
+  const int n_splits = a.n_splits > 1 ? a.n_splits : 1;
+  p.n_splits = n_splits;
+  p.tiles_per_split = (n_kt + n_splits - 1) / n_splits;
+  p.Nqp = nq_pad(a.Nq);
+  p.part_o = n_splits > 1 ? a.part : nullptr;
+  p.part_lse = n_splits > 1 ? a.part + static_cast<size_t>(n_splits) * a.B * a.H * p.Nqp * D : nullptr;
+  const long long blocks = static_cast<long long>(p.n_pairs) * a.B * a.H * n_splits;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   if constexpr (kSepP<D>) {
     using CS = FwdSpCfg<D>;
@@ -896,6 +1017,23 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     kern<<<static_cast<unsigned>(blocks), C::THREADS, C::SMEM, stream>>>(tq, tk, tv, p);
   }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || n_splits == 1) return e;
+  MergeParams mp;
+  mp.part_o = p.part_o;
+  mp.part_lse = p.part_lse;
+  mp.n_splits = n_splits;
+  mp.BH = a.B * a.H;
+  mp.H = a.H;
+  mp.Nq = a.Nq;
+  mp.Nqp = p.Nqp;
+  mp.o = p.o;
+  mp.o_sb = p.o_sb;
+  mp.o_sh = p.o_sh;
+  mp.o_ss = p.o_ss;
+  mp.lse = a.lse;
+  const long long rows = static_cast<long long>(mp.BH) * a.Nq;
+  fwd_merge_kernel<D, BF16><<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(mp);
   return cudaGetLastError();
 }
 

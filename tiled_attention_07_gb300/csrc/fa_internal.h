@@ -22,6 +22,10 @@ struct FwdArgs {
   int causal;
   bool bf16;
   int* err;  // device error word
+  // Split-KV (n_splits > 1): partial O_s then lse_s of every split, float32,
+  // [n_splits][B*H][nq_pad(Nq)][d] and [n_splits][B*H][nq_pad(Nq)].
+  int n_splits = 1;
+  float* part = nullptr;
 };
 
 struct BwdArgs {

@@ -48,6 +48,9 @@ FA_BWD_DQ = 3
 EXPORTED_SYMBOLS = (
     "fa_fwd",
     "fa_fwd_strided",
+    "fa_fwd_split_workspace_bytes",
+    "fa_fwd_split_count",
+    "fa_fwd_split",
     "fa_bwd_workspace_bytes",
     "fa_bwd",
     "fa_bwd_strided",
@@ -95,6 +98,13 @@ def lib() -> ctypes.CDLL:
         L.fa_fwd.restype = i
         L.fa_fwd_strided.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, ctypes.POINTER(Layout), vp]
         L.fa_fwd_strided.restype = i
+        L.fa_fwd_split_workspace_bytes.argtypes = [i, i, i, i, i]
+        L.fa_fwd_split_workspace_bytes.restype = ctypes.c_size_t
+        L.fa_fwd_split_count.argtypes = [i, i, i, i, i, i]
+        L.fa_fwd_split_count.restype = i
+        L.fa_fwd_split.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, ctypes.POINTER(Layout), i, vp,
+                                   ctypes.c_size_t, vp]
+        L.fa_fwd_split.restype = i
         L.fa_bwd_workspace_bytes.argtypes = [i, i, i, i, i]
         L.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
         L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, ctypes.c_size_t, vp]
@@ -196,6 +206,39 @@ def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, l
                               int(bool(causal)), dt, ctypes.byref(lay), _stream(stream))
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd")
+
+
+def fa_fwd_split_workspace_bytes(B: int, H: int, Nq: int, d: int, n_splits: int) -> int:
+    return int(lib().fa_fwd_split_workspace_bytes(B, H, Nq, d, n_splits))
+
+
+def fa_fwd_split_count(B: int, H: int, Nq: int, Nk: int, d: int, causal: bool) -> int:
+    return int(lib().fa_fwd_split_count(B, H, Nq, Nk, d, int(bool(causal))))
+
+
+def fa_fwd_split(q, k, v, o, lse, sm_scale: float, causal: bool, n_splits: int,
+                 workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """fa_fwd over ``n_splits`` key ranges merged by their log-sum-exps.
+
+    ``workspace`` is a CUDA byte tensor of at least
+    ``fa_fwd_split_workspace_bytes`` (unused when ``n_splits == 1``)."""
+    _check_cuda(q, k, v, o, lse)
+    B, H, Nq, d = _dims(q)
+    _, _, Nk, _ = _dims(k)
+    dt = _dtype_code(q)
+    if lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 tensor [B, H, Nq]")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        _check_cuda(workspace)
+        ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    lay = Layout()
+    lay.q, lay.k, lay.v, lay.o = _strides(q), _strides(k), _strides(v), _strides(o)
+    rc = lib().fa_fwd_split(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d, float(sm_scale),
+                            int(bool(causal)), dt, ctypes.byref(lay), int(n_splits), ws_ptr, ws_bytes,
+                            _stream(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_split")
 
 
 def fa_bwd_workspace_bytes(B: int, H: int, Nq: int, Nk: int, d: int) -> int:
