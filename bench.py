@@ -51,6 +51,8 @@ def parse_args(argv=None):
     ap.add_argument("--fwd-only", action="store_true",
                     help="time only the forward of --workload (the forward-only configurations), one JSON line")
     ap.add_argument("--split", default="1", help="with --fwd-only: key-range splits (an integer, or 'auto')")
+    ap.add_argument("--softmax", default=None, metavar="WORKLOAD",
+                    help="time the row-softmax kernel on a named softmax workload instead, one JSON line")
     ap.add_argument("--source-hash", default=None, metavar="KERNEL",
                     help="print the source hash that a traffic line for KERNEL must carry, and exit")
     return ap.parse_args(argv)
@@ -407,6 +409,69 @@ def run_fwd_only(args):
         print(json.dumps(line), flush=True)
 
 
+def run_softmax(args):
+    """fa_softmax_rows on one of the named row-softmax workloads: GB/s of the
+    algorithmic bytes (every element read once and written once) against
+    the measured HBM copy bandwidth.  Inputs smaller than 256 MB are made
+    cold by a scratch write between steps, outside the timed kernels."""
+    import torch
+
+    from tiled_attention_07_gb300 import fa
+    from tiled_attention_07_gb300 import workloads as W
+
+    rank, world = dist_init("nccl")
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = W.SOFTMAX_WORKLOADS[args.softmax]
+    x = W.softmax_inputs(w.rows, w.T, w.dtype, w.std, w.seed, device="cuda")
+    z = torch.empty_like(x)
+    lse = torch.empty(w.rows, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    nbytes = w.bytes_moved()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if nbytes / 2 < (256 << 20) else None
+    for _ in range(max(args.warmup, 3)):
+        fa.fa_softmax_rows(x, z, lse, stream)
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    clocks = ClockSampler() if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize(dev)
+    for i in range(K):
+        if flush is not None:
+            flush.fill_(i & 255)
+        evs[i][0].record(stream)
+        fa.fa_softmax_rows(x, z, lse, stream)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clk = clocks.stop() if clocks else None
+    ms = reduce_max(sum(a.elapsed_time(b) for a, b in evs), dev)
+    ms_step = ms / K
+    gbs = nbytes / (ms_step / 1e3) / 1e9
+    peaks, peak_src = load_peaks()
+    peak = peaks["hbm_gbs"]
+    line = {
+        "metric": "row softmax GB/s (algorithmic bytes) on 1 GB300", "value": round(world * gbs, 1), "unit": "GB/s",
+        "n_gpus": world, "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded N(0, std^2) logits)",
+        "config": {"workload": w.name, "rows": w.rows, "T": w.T, "bytes_per_step": nbytes,
+                   "l2": "256 MB scratch write between steps" if flush is not None else "inputs larger than L2",
+                   "parallelism": f"replica x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "softmax_rows", "achieved": round(gbs, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(gbs / peak, 4), "traffic": None,
+                     "peak_source": f"{peak_src} copy bandwidth"},
+        "clocks": clk, "gpu_launches": K, "e2e": None, "cpu_baseline": None,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_e2e(args, w, host, dev, stream, world):
     """Same metric through the public API with host buffers: every step copies
     q, k, v, dO from pinned host memory, runs forward and backward, and copies
@@ -544,6 +609,8 @@ def main(argv=None):
         run_reference(args)
     elif args.fwd_only:
         run_fwd_only(args)
+    elif args.softmax:
+        run_softmax(args)
     else:
         run_ours(args)
     import torch.distributed as dist

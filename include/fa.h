@@ -72,7 +72,9 @@ typedef enum {
     FA_ERR_WORKSPACE = 5      /* backward workspace missing or too small       */
 } fa_status;
 
-typedef enum { FA_FP16 = 0, FA_BF16 = 1 } fa_dtype;
+/* Element types.  The attention entry points take FA_FP16 and FA_BF16 (other
+ * values give FA_ERR_UNSUPPORTED); fa_softmax_rows also takes FA_FP32. */
+typedef enum { FA_FP16 = 0, FA_BF16 = 1, FA_FP32 = 2 } fa_dtype;
 
 /* Element strides of one [B, H, seq, d] tensor; the d stride is always 1. */
 typedef struct {
@@ -230,6 +232,28 @@ FA_API fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, con
                          fa_dtype dtype, void* stream);
 
 /* Human-readable name of a status code (static string, never NULL). */
+/*
+ * fa_softmax_rows -- row-wise softmax of a [rows, T] matrix with the online
+ * max/sum recurrence ("Puzzles 8 Long Softmax": z_ij = softmax_j(x_i1..x_iT),
+ * stabilised by the row max; the max and sum loops merged by rescaling the
+ * running sum, sum' = sum * exp(m_old - m_new) + ..., exp taken as exp2 of
+ * log2(e) x).
+ *   x    [rows, T] in, row r at element offset r * x_row_stride
+ *   z    [rows, T] out (same dtype as x), row r at r * z_row_stride
+ *   lse  float32 [rows] out, natural log of sum_j exp(x_rj), or NULL
+ *   dtype: FA_FP32, FA_FP16 or FA_BF16; arithmetic is float32 (exp2 of
+ *          the hardware approximation), z is rounded to dtype.
+ * Every x_rj takes part (nothing is padded into the sum, also when T is not
+ * a multiple of any tile).  A row of -inf gives NaN, like the definition.
+ * Requirements: rows >= 0, T >= 1; x, z non-null and 16-byte aligned; row
+ * strides >= T, in bytes multiples of 16; z must not overlap x unless
+ * z == x with equal strides (in place).  rows == 0 is a no-op.
+ * Rows of up to 8 * 16384 elements are held on chip (one read and one write
+ * of every element); longer rows are read twice.  Asynchronous on `stream`.
+ */
+FA_API fa_status fa_softmax_rows(const void* x, void* z, float* lse, int rows, int T, int64_t x_row_stride,
+                          int64_t z_row_stride, fa_dtype dtype, void* stream);
+
 FA_API const char* fa_status_string(fa_status status);
 
 /*

@@ -176,3 +176,20 @@ def test_split_checks_count_workspace_and_args(L):
         setattr(lay, n, fa.Strides(1024 * 64, 1024 * 64, 64))
     lay.v = fa.Strides(1024 * 64, 1024 * 64, 60)   # 120-byte rows
     assert split(L, layout=ctypes.byref(lay)) == fa.FA_ERR_INVALID_ARG
+
+
+def test_softmax_rows_rejects_bad_arguments(L):
+    def sm(x=FAKE, z=FAKE + (1 << 24), lse=None, rows=4, T=100, xs=100, zs=100, dtype=fa.FA_FP32):
+        return L.fa_softmax_rows(x, z, lse, rows, T, xs, zs, dtype, None)
+    assert sm(dtype=3) == fa.FA_ERR_UNSUPPORTED
+    assert sm(T=0) == fa.FA_ERR_INVALID_ARG
+    assert sm(rows=-1) == fa.FA_ERR_INVALID_ARG
+    assert sm(xs=99) == fa.FA_ERR_INVALID_ARG            # stride shorter than a row
+    assert sm(xs=101, zs=101) == fa.FA_ERR_INVALID_ARG   # 404-byte rows: not 16-byte aligned
+    assert sm(dtype=fa.FA_BF16, xs=100, zs=100) == fa.FA_ERR_INVALID_ARG   # 200-byte rows
+    assert sm(x=None) == fa.FA_ERR_INVALID_ARG
+    assert sm(z=FAKE + 8) == fa.FA_ERR_INVALID_ARG
+    assert sm(lse=FAKE + 2) == fa.FA_ERR_INVALID_ARG
+    assert sm(z=FAKE + 16, T=96) == fa.FA_ERR_INVALID_ARG   # overlapping, not identical
+    assert sm(z=FAKE, xs=100, zs=104) == fa.FA_ERR_INVALID_ARG   # same base, other stride
+    assert sm(rows=0) == fa.FA_OK

@@ -40,6 +40,7 @@ FA_ERR_WORKSPACE = 5
 
 FA_FP16 = 0
 FA_BF16 = 1
+FA_FP32 = 2
 
 FA_BWD_PREPROCESS = 1
 FA_BWD_DKDV = 2
@@ -56,6 +57,7 @@ EXPORTED_SYMBOLS = (
     "fa_bwd_strided",
     "fa_bwd_phase",
     "fa_bwd_noalloc",
+    "fa_softmax_rows",
     "fa_status_string",
     "fa_last_device_error",
     "fa_inject_device_error",
@@ -117,6 +119,8 @@ def lib() -> ctypes.CDLL:
         L.fa_bwd_phase.restype = i
         L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
         L.fa_bwd_noalloc.restype = i
+        L.fa_softmax_rows.argtypes = [vp, vp, vp, i, i, ctypes.c_int64, ctypes.c_int64, i, vp]
+        L.fa_softmax_rows.restype = i
         L.fa_status_string.argtypes = [i]
         L.fa_status_string.restype = ctypes.c_char_p
         L.fa_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
@@ -357,3 +361,29 @@ def attention_backward(q, k, v, o, do, lse, sm_scale: float, causal: bool, works
     dv = torch.empty_like(v)
     fa_bwd(q, k, v, o, do, lse, dq, dk, dv, sm_scale, causal, workspace, stream)
     return dq, dk, dv
+
+
+_SOFTMAX_DTYPES = {torch.float32: FA_FP32, torch.float16: FA_FP16, torch.bfloat16: FA_BF16}
+
+
+def fa_softmax_rows(x: torch.Tensor, z: torch.Tensor, lse: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Row softmax of the 2-D CUDA tensor ``x`` ([rows, T], unit column
+    stride) into ``z`` (same shape and dtype; may be ``x`` itself), and the
+    natural-log row log-sum-exp into the float32 [rows] ``lse`` if given."""
+    _check_cuda(x, z, lse)
+    if x.dim() != 2 or z.shape != x.shape or z.dtype != x.dtype:
+        raise ValueError("x and z must be 2-D tensors of the same shape and dtype")
+    if x.dtype not in _SOFTMAX_DTYPES:
+        raise TypeError(f"unsupported dtype {x.dtype} (float32, float16 or bfloat16)")
+    if x.stride(1) != 1 or z.stride(1) != 1:
+        raise ValueError("rows must be contiguous (unit column stride)")
+    rows, T = x.shape
+    if lse is not None and (lse.dtype != torch.float32 or lse.numel() != rows or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous float32 tensor of `rows` elements")
+    # a single row's stride is never used: give the smallest valid one
+    one = -(-T * x.element_size() // 16) * 16 // x.element_size()
+    rc = lib().fa_softmax_rows(_ptr(x), _ptr(z), _ptr(lse) if lse is not None else None, rows, T,
+                               x.stride(0) if rows > 1 else one, z.stride(0) if rows > 1 else one,
+                               _SOFTMAX_DTYPES[x.dtype], _stream(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_softmax_rows")

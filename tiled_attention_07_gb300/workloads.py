@@ -150,3 +150,58 @@ def head_view(t: torch.Tensor, layout: str, b: int, h: int) -> torch.Tensor:
 def stat_view(t: torch.Tensor, layout: str, b: int, h: int) -> torch.Tensor:
     """The ``[Nq]`` row of a per-row statistic (LSE) stored as ``[B, H, Nq]``."""
     return t[b, h]
+
+
+# ---------------------------------------------------------------------------
+# row softmax ("Puzzles 8 Long Softmax") inputs
+# ---------------------------------------------------------------------------
+
+SOFTMAX_DTYPES = {"fp32": torch.float32, "fp16": torch.float16, "bf16": torch.bfloat16}
+
+
+@dataclasses.dataclass(frozen=True)
+class SoftmaxWorkload:
+    name: str
+    dtype: str      # "fp32" | "fp16" | "bf16"
+    rows: int
+    T: int
+    std: float      # logits ~ N(0, std^2)
+    seed: int
+
+    def bytes_moved(self) -> float:
+        """Algorithmic HBM bytes: every element read once and written once."""
+        e = torch.empty((), dtype=SOFTMAX_DTYPES[self.dtype]).element_size()
+        return 2.0 * e * self.rows * self.T
+
+
+SOFTMAX_WORKLOADS: Dict[str, SoftmaxWorkload] = {
+    w.name: w
+    for w in [
+        # the puzzle's own scale: a handful of rows, T not a tile multiple
+        SoftmaxWorkload("fp32_rows4_t200", "fp32", 4, 200, 1.0, 30),
+        # long rows: 4096 x 32768 float32 (512 MB each way), two slices per row
+        SoftmaxWorkload("fp32_rows4096_t32768", "fp32", 4096, 32768, 3.0, 31),
+        # very long rows: 16 rows of 1M bf16 logits (streamed, eight CTAs per row)
+        SoftmaxWorkload("bf16_rows16_t1048576", "bf16", 16, 1 << 20, 3.0, 32),
+    ]
+}
+
+
+def softmax_inputs(rows: int, T: int, dtype: str, std: float, seed: int, row_stride: Optional[int] = None,
+                   device: str = "cpu") -> torch.Tensor:
+    """Seeded [rows, T] logits drawn in fp32 from N(0, std^2) with a CPU
+    generator and rounded to the dtype; with ``row_stride`` the rows sit in
+    a wider buffer (the returned tensor is a view of its first T columns)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    x = torch.randn((rows, T), generator=g, dtype=torch.float32)
+    if std != 1.0:
+        x.mul_(std)
+    x = x.to(SOFTMAX_DTYPES[dtype])
+    if row_stride is not None and row_stride != T:
+        buf = torch.zeros((rows, row_stride), dtype=x.dtype)
+        buf[:, :T] = x
+        if device != "cpu":
+            buf = buf.to(device)   # moved whole: a view would be copied densely
+        return buf[:, :T]
+    return x.to(device) if device != "cpu" else x
