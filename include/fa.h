@@ -248,8 +248,10 @@ FA_API fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, con
  * Requirements: rows >= 0, T >= 1; x, z non-null and 16-byte aligned; row
  * strides >= T, in bytes multiples of 16; z must not overlap x unless
  * z == x with equal strides (in place).  rows == 0 is a no-op.
- * Rows of up to 8 * 16384 elements are held on chip (one read and one write
- * of every element); longer rows are read twice.  Asynchronous on `stream`.
+ * A row is split over a cluster of up to 16 CTAs (8 where the GPU cannot
+ * schedule 16) of at most 192 KB each: rows of up to 3 MB (1.5 MB) are held
+ * on chip, one read and one write of every element; longer rows are read
+ * twice.  Asynchronous on `stream`.
  */
 FA_API fa_status fa_softmax_rows(const void* x, void* z, float* lse, int rows, int T, int64_t x_row_stride,
                           int64_t z_row_stride, fa_dtype dtype, void* stream);

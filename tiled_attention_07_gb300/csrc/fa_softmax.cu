@@ -7,15 +7,15 @@
 // sum' = sum * exp(m1 - m2) + sum_j exp(x_j - m2).  exp is taken as exp2 of
 // log2(e) x, as the puzzle recommends.
 //
-// GB300 design: the row is cut into C <= 8 slices, one CTA each, launched as
-// one thread-block cluster per row.  A CTA reads its slice once with 16-byte
-// loads, keeps it in shared memory as float32 and keeps a running (max, sum)
-// per thread while it loads.  The threads' pairs are merged with the same
-// rescaling inside the CTA, then across the cluster through distributed
-// shared memory.  Each CTA finally writes z for its slice from shared memory,
-// so every element crosses HBM once in and once out.  Slices longer than the
-// shared-memory buffer are streamed: one pass for the (max, sum), a second
-// read for the output.
+// GB300 design: the row is cut into C <= 16 slices of about 64 KB, one CTA
+// each, launched as one thread-block cluster per row.  A CTA brings its slice
+// into shared memory with one bulk asynchronous copy (cp.async.bulk on an
+// mbarrier), keeps a running (max, sum) per thread over it, merges the
+// threads' pairs with the same rescaling, then merges the CTAs' pairs through
+// distributed shared memory.  It writes z over its slice in shared memory and
+// stores it with one bulk copy back to global memory, so every element crosses
+// HBM once in and once out.  Slices longer than the on-chip limit are streamed
+// from global memory: one pass for the (max, sum), a second read for z.
 #include "../../include/fa.h"
 #include "ptx.cuh"
 
@@ -23,12 +23,16 @@
 #include <cuda_fp16.h>
 #include <math_constants.h>
 
+#include <algorithm>
+
 namespace fa {
 namespace {
 
-constexpr int kSmThreads = 256;
-constexpr int kSlice = 16384;      // elements one CTA holds on chip (64 KB as float32)
-constexpr int kMaxCluster = 8;     // portable cluster size
+constexpr int kThreads = 256;
+constexpr int kTargetSliceBytes = 64 * 1024;   // slice size aimed at: three CTAs per SM
+constexpr int kMaxSliceBytes = 192 * 1024;     // the most one CTA holds on chip
+constexpr int kMaxCluster = 16;                // 8 is portable; 16 where the GPU can schedule it
+constexpr uint32_t kBulkChunk = 32768;         // bytes per bulk copy instruction
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct SoftmaxParams {
@@ -147,6 +151,7 @@ __device__ __forceinline__ float2 ld_cluster_f2(const void* local, uint32_t rank
 }
 
 // (max, sum) of the whole CTA from each thread's pair.
+template <int THREADS>
 __device__ __forceinline__ Stat block_stat(Stat st, Stat* red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -159,18 +164,18 @@ __device__ __forceinline__ Stat block_stat(Stat st, Stat* red) {
   if (lane == 0) red[warp] = st;
   __syncthreads();
   Stat r = red[0];
-  for (int w = 1; w < kSmThreads / 32; ++w) r = merge_stat(r, red[w]);
+  for (int w = 1; w < THREADS / 32; ++w) r = merge_stat(r, red[w]);
   __syncthreads();
   return r;
 }
 
-template <typename E>
-__global__ void __launch_bounds__(kSmThreads) softmax_rows_kernel(const SoftmaxParams p) {
+template <typename E, int THREADS>
+__global__ void __launch_bounds__(THREADS) softmax_rows_kernel(const SoftmaxParams p) {
   using V = Vec<E>;
   constexpr int N = V::N;
-  extern __shared__ float4 sm_buf4[];
-  float* buf = reinterpret_cast<float*>(sm_buf4);
-  __shared__ Stat red[kSmThreads / 32];
+  extern __shared__ __align__(128) uint8_t sm[];   // the slice, in the input type
+  __shared__ uint64_t bar;
+  __shared__ Stat red[THREADS / 32];
   __shared__ float2 cta_stat;   // this CTA's (max, sum), read by the rest of the cluster
 
   const int rank = p.C > 1 ? static_cast<int>(cluster_rank()) : 0;
@@ -182,24 +187,41 @@ __global__ void __launch_bounds__(kSmThreads) softmax_rows_kernel(const SoftmaxP
   const uint8_t* xr = reinterpret_cast<const uint8_t*>(p.x) + (static_cast<int64_t>(row) * p.xs + c0) * sizeof(E);
   uint8_t* zr = reinterpret_cast<uint8_t*>(p.z) + (static_cast<int64_t>(row) * p.zs + c0) * sizeof(E);
 
-  // pass 1: running (max, sum) per thread; the slice into shared memory
-  Stat st{-CUDART_INF_F, 0.f};
-  for (int i = threadIdx.x; i < nv; i += kSmThreads) {
-    float v[N];
-    V::load(xr + static_cast<size_t>(i) * 16, v);
-    if (p.resident) {
-#pragma unroll
-      for (int e = 0; e < N; e += 4)
-        *reinterpret_cast<float4*>(buf + i * N + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+  // The slice in bytes: a 16-byte multiple by bulk copy, the rest (the last
+  // slice's < 16-byte tail) through registers.
+  const uint32_t nbytes = static_cast<uint32_t>(n) * sizeof(E);
+  const uint32_t bulk = nbytes & ~15u;
+  const int t0 = static_cast<int>(bulk / sizeof(E));
+  if (p.resident) {
+    if (threadIdx.x == 0) {
+      mbar_init(&bar, 1);
+      fence_mbar_init();
     }
+    __syncthreads();
+    if (threadIdx.x == 0 && bulk > 0) {
+      mbar_arrive_expect_tx(&bar, bulk);
+      for (uint32_t off = 0; off < bulk; off += kBulkChunk)
+        bulk_load(sm + off, xr + off, min(kBulkChunk, bulk - off), &bar);
+    }
+    for (int e = t0 + threadIdx.x; e < n; e += THREADS)
+      reinterpret_cast<E*>(sm)[e] = reinterpret_cast<const E*>(xr)[e];
+    if (bulk > 0) mbar_wait_drain(&bar, 0);   // the copy always completes
+    __syncthreads();
+  }
+  const uint8_t* src = p.resident ? sm : xr;
+
+  // pass 1: running (max, sum) per thread
+  Stat st{-CUDART_INF_F, 0.f};
+  for (int i = threadIdx.x; i < nv; i += THREADS) {
+    float v[N];
+    V::load(src + static_cast<size_t>(i) * 16, v);
     st = fold<N>(st, v);
   }
-  for (int e = nv * N + threadIdx.x; e < n; e += kSmThreads) {
-    const float v1[1] = {V::get(xr, e)};
-    if (p.resident) buf[e] = v1[0];
+  for (int e = nv * N + threadIdx.x; e < n; e += THREADS) {
+    const float v1[1] = {V::get(src, e)};
     st = fold<1>(st, v1);
   }
-  Stat tot = block_stat(st, red);
+  Stat tot = block_stat<THREADS>(st, red);
   if (p.C > 1) {
     if (threadIdx.x == 0) cta_stat = make_float2(tot.m, tot.s);
     cluster_arrive();
@@ -214,54 +236,84 @@ __global__ void __launch_bounds__(kSmThreads) softmax_rows_kernel(const SoftmaxP
   }
   if (rank == 0 && threadIdx.x == 0 && p.lse != nullptr) p.lse[row] = tot.m + logf(tot.s);
 
-  // pass 2: z = exp(x - max) / sum
+  // pass 2: z = exp(x - max) / sum, over the slice in shared memory (then one
+  // bulk store) or straight to global memory when streaming
   const float inv = 1.f / tot.s;
   const float mx = tot.m;
-  for (int i = threadIdx.x; i < nv; i += kSmThreads) {
+  uint8_t* dst = p.resident ? sm : zr;
+  for (int i = threadIdx.x; i < nv; i += THREADS) {
     float v[N];
-    if (p.resident) {
-#pragma unroll
-      for (int e = 0; e < N; e += 4) {
-        const float4 w = *reinterpret_cast<const float4*>(buf + i * N + e);
-        v[e] = w.x;
-        v[e + 1] = w.y;
-        v[e + 2] = w.z;
-        v[e + 3] = w.w;
-      }
-    } else {
-      V::load(xr + static_cast<size_t>(i) * 16, v);
-    }
+    V::load(src + static_cast<size_t>(i) * 16, v);
 #pragma unroll
     for (int e = 0; e < N; ++e) v[e] = ex2_approx((v[e] - mx) * kLog2e) * inv;
-    V::store(zr + static_cast<size_t>(i) * 16, v);
+    V::store(dst + static_cast<size_t>(i) * 16, v);
   }
-  for (int e = nv * N + threadIdx.x; e < n; e += kSmThreads) {
-    const float x = p.resident ? buf[e] : V::get(xr, e);
-    V::put(zr, e, ex2_approx((x - mx) * kLog2e) * inv);
+  for (int e = nv * N + threadIdx.x; e < n; e += THREADS) V::put(dst, e, ex2_approx((V::get(src, e) - mx) * kLog2e) * inv);
+  if (p.resident) {
+    fence_proxy_async_smem();   // z in shared memory, visible to the bulk copy
+    __syncthreads();
+    if (threadIdx.x == 0 && bulk > 0) {
+      for (uint32_t off = 0; off < bulk; off += kBulkChunk) bulk_store(zr + off, sm + off, min(kBulkChunk, bulk - off));
+      bulk_commit_group();
+    }
+    for (int e = t0 + threadIdx.x; e < n; e += THREADS)
+      reinterpret_cast<E*>(zr)[e] = reinterpret_cast<const E*>(sm)[e];
+    if (threadIdx.x == 0 && bulk > 0) bulk_wait_group0();   // shared memory is read before the CTA exits
   }
   // No CTA may exit while another still reads its shared memory.
   if (p.C > 1) cluster_wait();
 }
 
-template <typename E>
-cudaError_t launch_softmax(const SoftmaxParams& p, cudaStream_t stream) {
-  auto kern = softmax_rows_kernel<E>;
-  const int smem = p.resident ? static_cast<int>(p.per * sizeof(float)) : 0;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSlice * 4);
+template <typename E, int THREADS>
+cudaError_t launch_softmax_t(SoftmaxParams p, cudaStream_t stream) {
+  auto kern = softmax_rows_kernel<E, THREADS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSliceBytes);
   if (e != cudaSuccess) return e;
+  const int C = p.C;
+  auto slice = [&](int c) {
+    const int64_t per = (static_cast<int64_t>(p.T) + c - 1) / c;
+    p.C = c;
+    p.per = static_cast<int>((per + 7) / 8 * 8);
+    p.resident = static_cast<int64_t>(p.per) * sizeof(E) <= kMaxSliceBytes;
+  };
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(static_cast<long long>(p.rows) * p.C));
-  cfg.blockDim = dim3(kSmThreads);
-  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-  cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(p.C);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  auto config = [&]() {
+    cfg.gridDim = dim3(static_cast<unsigned>(static_cast<long long>(p.rows) * p.C));
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = p.resident ? static_cast<size_t>(p.per) * sizeof(E) : 0;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(p.C);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  };
+  slice(C);
+  if (C > 8) {
+    // A cluster of more than 8 CTAs is not portable: use it only where this
+    // GPU can schedule one with this much shared memory.
+    int n_clusters = 0;
+    config();
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&n_clusters, kern, &cfg) != cudaSuccess || n_clusters < 1) {
+      (void)cudaGetLastError();
+      slice(8);
+    }
+  }
+  config();
   return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+// Slices of about kTargetSliceBytes over a cluster of up to kMaxCluster CTAs.
+template <typename E>
+cudaError_t launch_softmax(SoftmaxParams p, cudaStream_t stream) {
+  const int64_t row_bytes = static_cast<int64_t>(p.T) * sizeof(E);
+  p.C = static_cast<int>(std::min<int64_t>(kMaxCluster, (row_bytes + kTargetSliceBytes - 1) / kTargetSliceBytes));
+  // 256 threads measured fastest for both 64 KB and 128 KB slices (512 and
+  // 1024 were slower on GB300).
+  return launch_softmax_t<E, kThreads>(p, stream);
 }
 
 }  // namespace
@@ -297,11 +349,6 @@ extern "C" fa_status fa_softmax_rows(const void* x, void* z, float* lse, int row
   p.T = T;
   p.xs = x_row_stride;
   p.zs = z_row_stride;
-  const int64_t slices = (static_cast<int64_t>(T) + kSlice - 1) / kSlice;
-  p.C = static_cast<int>(slices < kMaxCluster ? slices : kMaxCluster);
-  const int64_t per = (static_cast<int64_t>(T) + p.C - 1) / p.C;
-  p.per = static_cast<int>((per + 7) / 8 * 8);
-  p.resident = p.per <= kSlice;
   cudaError_t e;
   switch (dtype) {
     case FA_FP32: e = launch_softmax<float>(p, static_cast<cudaStream_t>(stream)); break;
