@@ -144,14 +144,16 @@ struct BwdCfg {
 // first 16 columns of its own 32-column quarter.
 __device__ __forceinline__ uint32_t split_a_col(int ks) { return (ks >> 1) * 32 + (ks & 1) * 8; }
 
-// M = 128 x N = 128 x K = D, both operands K-major in swizzled tiles.
-template <int D>
+// M = 128 x N = 128 x K = 16 KS (default: D), both operands K-major in
+// swizzled tiles.  KS > D / 16 takes in the tiles' padding columns too.
+template <int D, int KS = D / 16>
 __device__ __forceinline__ void mma_nt(uint32_t d_tmem, uint32_t a_addr, uint32_t b_addr, uint32_t idesc) {
   using G = TileGeo<D>;
+  static_assert(16 * KS <= G::NCH * G::CC, "K-steps beyond the tile");
   const uint64_t ad0 = make_sdesc(a_addr, 16, G::SBO, G::LAYOUT);
   const uint64_t bd0 = make_sdesc(b_addr, 16, G::SBO, G::LAYOUT);
 #pragma unroll
-  for (int ks = 0; ks < D / 16; ++ks) {
+  for (int ks = 0; ks < KS; ++ks) {
     const uint32_t off = (ks / G::KPC) * G::CHB + (ks % G::KPC) * 32;
     if (elect_one()) umma_ss(d_tmem, desc_add(ad0, off), desc_add(bd0, off), idesc, ks > 0);
   }
@@ -170,6 +172,30 @@ __device__ __forceinline__ void mma_tn(uint32_t d_tmem, uint32_t a_tmem, uint32_
     const uint32_t acol = kContiguousA ? static_cast<uint32_t>(ks * 8) : split_a_col(ks);
     if (elect_one()) umma_ts(d_tmem, a_tmem + acol, desc_add(bd0, ks * 16 * G::ROWB), idesc, (acc || ks > 0) ? 1u : 0u);
   }
+}
+
+// Folding L and D into the GEMMs (bf16, d = 80): the tiles of d = 80 carry
+// 16 zero-filled padding columns [80, 96).  With 1 in columns 80 and 81 of K
+// and V, and a two-term bf16 split of -L log2(e) / c and of -D in columns 80
+// and 81 of Q_i and dO_i, the padded GEMMs give
+//   K Q_i^T (96 columns) = S^T - L log2(e) / c,   V dO_i^T = dP^T - D,
+// so that P^T = exp2(c (S^T)') and dS^T = P^T o (dP^T)': the elementwise
+// warps read no L or D.  The split a = bf16(v), b = bf16(v - a) keeps v to
+// about 2^-16 relatively; v = -inf (padded query rows) gives a = -inf, b = 0.
+// The write goes to (row r, columns 80-81) of a tile stored as 32-column
+// chunks with 64-byte rows and the 64-byte swizzle: chunk 2, 16-byte granule
+// 2 ^ ((r / 2) % 4) of row r.
+constexpr int kFoldKSteps = 6;
+
+__device__ __forceinline__ uint32_t* fold_slot(uint8_t* tile, int r) {
+  using G = TileGeo<80>;
+  return reinterpret_cast<uint32_t*>(tile + 2 * G::CHB + r * G::ROWB + ((2 ^ ((r >> 1) & 3)) << 4));
+}
+
+__device__ __forceinline__ uint32_t bf16_split(float v) {
+  if (!(v > -CUDART_INF_F)) return pack2<true>(v, 0.f);   // -inf: (-inf, 0)
+  const float a = __bfloat162float(__float2bfloat16_rn(v));
+  return pack2<true>(a, v - a);
 }
 
 struct MainParams {
@@ -220,6 +246,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   constexpr int NS = C::KV_NSTAGE;
   // kSepP: P^T has a 64-column region of its own (see above).
   constexpr bool kSepP = 256 + 2 * D + 64 <= 512;
+  // kFold: L and D folded into the padded GEMMs (see fold_slot).
+  constexpr bool kFold = BF16 && D == 80 && kSepP;
+  constexpr int KS = kFold ? kFoldKSteps : D / 16;
   constexpr uint32_t kColDV = 256;
   constexpr uint32_t kColDK = kSepP ? 256 + D : 384;
   constexpr uint32_t kColP = kSepP ? 256 + 2 * D : 0;
@@ -240,7 +269,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   uint64_t* bar_drain = bar_acc + 1;  // every MMA of both issuers complete
   uint64_t* bar_sfree = bar_drain + 1;  // S^T read into registers (separate-P^T layout)
   uint64_t* bar_dvd = bar_sfree + 1;    // dV_i complete: P^T_i consumed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_dvd + 1);
+  uint64_t* bar_ext = bar_dvd + 1;      // folded columns of K, V, Q_0, dO_0 written (kFold)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_ext + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -270,6 +300,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     mbar_init(bar_drain, 2);
     mbar_init(bar_sfree, C::EW_WARPS);
     mbar_init(bar_dvd, 1);
+    mbar_init(bar_ext, C::EW_WARPS);
     fence_mbar_init();
   }
   if (warp == C::MMA_WARP) {
@@ -325,6 +356,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       const uint32_t sv = smem_u32(sV);
       const uint32_t sst = smem_u32(sStage);
       mbar_wait(bar_kv, 0, p.err, 22);
+      if (kFold) mbar_wait(bar_ext, 0, p.err, 36);
       __syncwarp();
       for (int it = 0; it < n_it; ++it) {
         const int s = it % NS;
@@ -338,7 +370,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             // S^T_i was issued one step ahead (below); issue S^T_{i+1} as soon
             // as the elementwise warps hold S^T_i in registers.
             if (it == 0) {
-              mma_nt<D>(tmem, sk, sq, idesc_nt);          // S^T_0 = K Q_0^T
+              mma_nt<D, KS>(tmem, sk, sq, idesc_nt);      // S^T_0 = K Q_0^T
               if (elect_one()) umma_commit(bar_s);
             }
             if (it + 1 < n_it) {
@@ -347,7 +379,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
               mbar_wait(bar_sfree, it & 1, p.err, 31);
               __syncwarp();
               tc_fence_after();
-              mma_nt<D>(tmem, sk, sst + s1 * C::KV_STAGE, idesc_nt);   // S^T_{i+1}
+              mma_nt<D, KS>(tmem, sk, sst + s1 * C::KV_STAGE, idesc_nt);   // S^T_{i+1}
               if (elect_one()) umma_commit(bar_s);
             }
             mbar_wait(bar_pt, it & 1, p.err, 24);
@@ -364,7 +396,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
             mma_tn<D>(tmem + kColDV, tmem, sdo, idesc_tn, it > 0);  // dV += P^T_i dO_i
           }
         } else {
-          mma_nt<D>(tmem + 128, sv, sdo, idesc_nt);       // dP^T_i = V dO_i^T
+          mma_nt<D, KS>(tmem + 128, sv, sdo, idesc_nt);   // dP^T_i = V dO_i^T
           if (elect_one()) umma_commit(bar_dp);
           mbar_wait(bar_ds, it & 1, p.err, 26);
           __syncwarp();
@@ -390,6 +422,28 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const uint32_t tdP = tmem + lane_off + 128 + g * 32;
     const uint32_t tP = tmem + lane_off + kColP + g * (kSepP ? 16 : 32);
     const uint64_t cs2 = f2pack(p.scale_log2, p.scale_log2);
+    const int kr = quad * 32 + lane;   // this thread's row of the K/V tile and of the stage rows it folds
+
+    // Folded columns of stage s: Q rows by warpgroup 2 (-L log2 e / c), dO
+    // rows by warpgroup 3 (-D); L and D come with the stage.
+    auto fold_stage = [&](int s) {
+      uint8_t* st = sStage + s * C::KV_STAGE;
+      const float* l = reinterpret_cast<const float*>(st + 2 * C::TILE);
+      if (g == 2) *fold_slot(st, kr) = bf16_split(l[kr] / p.scale_log2);
+      if (g == 3) *fold_slot(st + C::TILE, kr) = bf16_split(-l[128 + kr]);
+    };
+    if (kFold) {
+      if (n_it > 0) {
+        mbar_wait(bar_kv, 0, p.err, 37);
+        mbar_wait(&bar_full[0], 0, p.err, 38);
+        if (g == 0) *fold_slot(sK, kr) = 0x3F803F80u;   // bf16 (1, 1)
+        if (g == 1) *fold_slot(sV, kr) = 0x3F803F80u;
+        fold_stage(0);
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_ext);
+    }
 
     for (int it = 0; it < n_it; ++it) {
       const int s = it % NS;
@@ -411,6 +465,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         for (int e = 0; e < 32; ++e) pt[e] = __uint_as_float(r[e]);
       }
       if (kSepP) {
+        if (kFold && it + 1 < n_it) {
+          // stage i+1's folded columns, before S^T_{i+1} may be issued
+          const int s1 = (it + 1) % NS;
+          mbar_wait(&bar_full[s1], ((it + 1) / NS) & 1, p.err, 39);
+          fold_stage(s1);
+          fence_proxy_async_smem();
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_sfree);   // S^T_i is in registers
@@ -418,10 +479,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       // P^T = exp2(c S^T - L log2 e); sL holds -L log2 e
 #pragma unroll
       for (int e = 0; e < 32; e += 4) {
-        const float4 nl = *reinterpret_cast<const float4*>(sL + e);
         float x0, x1, x2, x3;
-        f2unpack(ffma2(f2pack(pt[e], pt[e + 1]), cs2, f2pack(nl.x, nl.y)), x0, x1);
-        f2unpack(ffma2(f2pack(pt[e + 2], pt[e + 3]), cs2, f2pack(nl.z, nl.w)), x2, x3);
+        if (kFold) {   // -L log2 e is already in S^T
+          f2unpack(fmul2(f2pack(pt[e], pt[e + 1]), cs2), x0, x1);
+          f2unpack(fmul2(f2pack(pt[e + 2], pt[e + 3]), cs2), x2, x3);
+        } else {
+          const float4 nl = *reinterpret_cast<const float4*>(sL + e);
+          f2unpack(ffma2(f2pack(pt[e], pt[e + 1]), cs2, f2pack(nl.x, nl.y)), x0, x1);
+          f2unpack(ffma2(f2pack(pt[e + 2], pt[e + 3]), cs2, f2pack(nl.z, nl.w)), x2, x3);
+        }
         pt[e] = ex2_approx(x0);
         pt[e + 1] = ex2_approx(x1);
         pt[e + 2] = ex2_approx(x2);
@@ -457,14 +523,21 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
-          const float4 dd = *reinterpret_cast<const float4*>(sD + e);
           float a0, a1, a2, a3;
-          f2unpack(fmul2(fsub2(f2pack(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), f2pack(dd.x, dd.y)),
-                         f2pack(pt[e], pt[e + 1])),
-                   a0, a1);
-          f2unpack(fmul2(fsub2(f2pack(__uint_as_float(r[e + 2]), __uint_as_float(r[e + 3])), f2pack(dd.z, dd.w)),
-                         f2pack(pt[e + 2], pt[e + 3])),
-                   a2, a3);
+          if (kFold) {   // -D is already in dP^T
+            f2unpack(fmul2(f2pack(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), f2pack(pt[e], pt[e + 1])),
+                     a0, a1);
+            f2unpack(fmul2(f2pack(__uint_as_float(r[e + 2]), __uint_as_float(r[e + 3])), f2pack(pt[e + 2], pt[e + 3])),
+                     a2, a3);
+          } else {
+            const float4 dd = *reinterpret_cast<const float4*>(sD + e);
+            f2unpack(fmul2(fsub2(f2pack(__uint_as_float(r[e]), __uint_as_float(r[e + 1])), f2pack(dd.x, dd.y)),
+                           f2pack(pt[e], pt[e + 1])),
+                     a0, a1);
+            f2unpack(fmul2(fsub2(f2pack(__uint_as_float(r[e + 2]), __uint_as_float(r[e + 3])), f2pack(dd.z, dd.w)),
+                           f2pack(pt[e + 2], pt[e + 3])),
+                     a2, a3);
+          }
           pk[e / 2] = pack2<BF16>(a0, a1);
           pk[e / 2 + 1] = pack2<BF16>(a2, a3);
         }
