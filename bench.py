@@ -45,7 +45,7 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=None, help="workload name (default: the fwd+bwd bench workload)")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch size (small profiling cases)")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--fwd-only", action="store_true",
@@ -475,50 +475,92 @@ def run_softmax(args):
 def run_e2e(args, w, host, dev, stream, world):
     """Same metric through the public API with host buffers: every step copies
     q, k, v, dO from pinned host memory, runs forward and backward, and copies
-    O, LSE, dQ, dK, dV back to pinned host memory."""
+    O, LSE, dQ, dK, dV back to pinned host memory.
+
+    The steps are pipelined the way a stream of batches would be: two sets of
+    device (and host output) buffers, the host-to-device copies on one stream,
+    the kernels on another, the device-to-host copies on a third; step i's
+    inputs are copied while step i-1 computes and step i-2's results go back.
+    The forward starts once q, k, v are in (dO is still on its way) and O, LSE
+    go back while the backward runs.  Events order every reuse of a buffer set.
+    The timed region runs from the first copy in to the last copy out, so the
+    pipeline's fill and drain are inside it."""
     import torch
 
     from tiled_attention_07_gb300 import fa
 
     pin = {k: t.pin_memory() for k, t in host.items()}
-    dx = {k: torch.empty_like(t, device=dev) for k, t in host.items()}
-    q, k, v, do = dx["q"], dx["k"], dx["v"], dx["do"]
-    o = torch.empty_like(q)
-    lse = torch.empty(fa.lse_shape(q), dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    B, H, Nq, d = fa._dims(q)
-    Nk = fa._dims(k)[2]
-    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, Nq, Nk, d), dtype=torch.uint8, device=dev)
-    outs = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
-    hout = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in outs.items()}
-
-    def step():
-        for n in ("q", "k", "v", "do"):
-            dx[n].copy_(pin[n], non_blocking=True)
-        fa.fa_fwd(q, k, v, o, lse, w.sm_scale, w.causal, stream)
-        fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, w.sm_scale, w.causal, ws, stream)
-        for n, t in outs.items():
-            hout[n].copy_(t, non_blocking=True)
-
+    B, H, Nq, d = fa._dims(host["q"])
+    Nk = fa._dims(host["k"])[2]
+    s_in = torch.cuda.Stream(dev)
+    s_out = torch.cuda.Stream(dev)
+    sets = []
     for _ in range(2):
-        step()
+        dx = {k: torch.empty_like(t, device=dev) for k, t in host.items()}
+        outs = {"o": torch.empty_like(dx["q"]),
+                "lse": torch.empty(fa.lse_shape(dx["q"]), dtype=torch.float32, device=dev),
+                "dq": torch.empty_like(dx["q"]), "dk": torch.empty_like(dx["k"]), "dv": torch.empty_like(dx["v"])}
+        sets.append({
+            "x": dx, "out": outs,
+            "ws": torch.empty(fa.fa_bwd_workspace_bytes(B, H, Nq, Nk, d), dtype=torch.uint8, device=dev),
+            "hout": {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in outs.items()},
+            "ev_in_fwd": torch.cuda.Event(), "ev_in": torch.cuda.Event(), "ev_fwd": torch.cuda.Event(),
+            "ev_cmp": torch.cuda.Event(), "ev_out": torch.cuda.Event(), "used": False,
+        })
+
+    def step(i):
+        S = sets[i % 2]
+        x, out = S["x"], S["out"]
+        if S["used"]:
+            s_in.wait_event(S["ev_cmp"])      # step i-2's kernels are done with these inputs
+        with torch.cuda.stream(s_in):
+            for n in ("q", "k", "v"):
+                x[n].copy_(pin[n], non_blocking=True)
+            S["ev_in_fwd"].record(s_in)       # the forward needs no dO
+            x["do"].copy_(pin["do"], non_blocking=True)
+            S["ev_in"].record(s_in)
+        stream.wait_event(S["ev_in_fwd"])
+        if S["used"]:
+            stream.wait_event(S["ev_out"])    # step i-2's results have left these outputs
+        fa.fa_fwd(x["q"], x["k"], x["v"], out["o"], out["lse"], w.sm_scale, w.causal, stream)
+        S["ev_fwd"].record(stream)
+        stream.wait_event(S["ev_in"])
+        fa.fa_bwd(x["q"], x["k"], x["v"], out["o"], x["do"], out["lse"], out["dq"], out["dk"], out["dv"],
+                  w.sm_scale, w.causal, S["ws"], stream)
+        S["ev_cmp"].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(S["ev_fwd"])     # O and LSE go back while the backward runs
+            for n in ("o", "lse"):
+                S["hout"][n].copy_(out[n], non_blocking=True)
+            s_out.wait_event(S["ev_cmp"])
+            for n in ("dq", "dk", "dv"):
+                S["hout"][n].copy_(out[n], non_blocking=True)
+            S["ev_out"].record(s_out)
+        S["used"] = True
+
+    for i in range(2):
+        step(i)
     torch.cuda.synchronize(dev)
     K = max(1, args.e2e_steps)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     barrier()
-    t0.record(stream)
-    for _ in range(K):
-        step()
-    t1.record(stream)
+    s_in.wait_stream(stream)
+    s_in.wait_stream(s_out)
+    t0.record(s_in)
+    for i in range(K):
+        step(i)
+    s_out.wait_stream(stream)
+    t1.record(s_out)
     torch.cuda.synchronize(dev)
     barrier()
     ms = reduce_max(t0.elapsed_time(t1), dev)
     value = world * K * (w.fwd_flops() + w.bwd_flops()) / (ms / 1e3) / 1e12
     bi = sum(t.numel() * t.element_size() for t in pin.values())
-    bo = sum(t.numel() * t.element_size() for t in hout.values())
+    bo = sum(t.numel() * t.element_size() for t in sets[0]["hout"].values())
     return {"value": round(value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-            "steps": K, "ms_per_step": round(ms / K, 3)}
+            "steps": K, "ms_per_step": round(ms / K, 3),
+            "pipeline": "2 buffer sets; copies in, kernels, copies out on 3 streams"}
 
 
 # ---------------------------------------------------------------------------
