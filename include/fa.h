@@ -152,6 +152,32 @@ FA_API fa_status fa_fwd_split(const void* q, const void* k, const void* v, void*
                        size_t workspace_bytes, void* stream);
 
 /*
+ * fa_fwd_fp8v -- the forward with V in float8 e5m2 ("Understanding Triton
+ * Tutorials Part 2", "Fused Attention 2": when V is float8_e5m2 it is stored
+ * transposed, and the probabilities of each key block are cast to float8 e5m2
+ * before the product with V; the row sum l takes the unrounded p).
+ *   q   [B, H, Nq, d]  in  (dtype)       k  [B, H, Nk, d]  in  (dtype)
+ *   vt  [B, H, d, vt_ld] e5m2 codes (one byte each), in: key j of head
+ *       dimension c of head (b, h) at byte ((b*H + h)*d + c)*vt_ld + j;
+ *       vt_ld >= Nk, vt_ld % 16 == 0, vt 16-byte aligned; bytes j >= Nk of a
+ *       row are not read.
+ *   o   [B, H, Nq, d]  out (dtype)       lse [B, H, Nq] float32 out
+ * q, k and o are contiguous; dtype (FA_FP16 or FA_BF16) is theirs.  S = q k^T
+ * runs on the 16-bit tensor-core path; P is rounded to e5m2 (to nearest
+ * even, saturating) and O += P V runs on the 8-bit path (kind::f8f6f4) with
+ * float32 accumulation.  LSE is exact, as in fa_fwd; O differs from the
+ * exact result by at most about 2^-3 * max |v| over the row's keys (the
+ * rounding of P, relative 2^-3) plus the 16-bit rounding of O.
+ * d in {64, 80}; d = 128 gives FA_ERR_UNSUPPORTED (with d = 128 the tensor
+ * memory has no room for P next to S and O of two query tiles).  Errors as
+ * fa_fwd; vt_ld out of range gives FA_ERR_INVALID_ARG.  One launch on
+ * `stream`.
+ */
+FA_API fa_status fa_fwd_fp8v(const void* q, const void* k, const void* vt, void* o, float* lse,
+                      int B, int H, int Nq, int Nk, int d, int64_t vt_ld, float sm_scale,
+                      int causal, fa_dtype dtype, void* stream);
+
+/*
  * fa_bwd_workspace_bytes -- size of the scratch buffer fa_bwd needs: the
  * per-row D = rowsum(O o dO) and the log2-domain LSE, float32, padded to
  * whole 128-row query tiles: 2 * 4 * B*H*ceil(Nq/128)*128 bytes.

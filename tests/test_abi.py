@@ -82,6 +82,33 @@ def test_fwd_rejects_bad_arguments(L, kw, code):
     assert fwd(L, **kw) == code
 
 
+def fwd8(L, q=FAKE, k=FAKE, vt=FAKE, o=FAKE, lse=FAKE, B=1, H=1, Nq=128, Nk=128, d=64, ld=128, scale=0.125,
+         causal=0, dtype=fa.FA_FP16):
+    return L.fa_fwd_fp8v(q, k, vt, o, lse, B, H, Nq, Nk, d, ld, scale, causal, dtype, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=128), fa.FA_ERR_UNSUPPORTED),       # no room for P next to S and O
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(dtype=fa.FA_FP32), fa.FA_ERR_UNSUPPORTED),
+    (dict(Nk=100, ld=100), fa.FA_ERR_INVALID_ARG),   # row stride not a multiple of 16 bytes
+    (dict(Nk=128, ld=112), fa.FA_ERR_INVALID_ARG),   # rows shorter than Nk
+    (dict(vt=None), fa.FA_ERR_INVALID_ARG),
+    (dict(vt=FAKE + 8), fa.FA_ERR_INVALID_ARG),
+    (dict(q=FAKE + 2), fa.FA_ERR_INVALID_ARG),
+    (dict(lse=None), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(Nk=0, ld=16), fa.FA_ERR_INVALID_ARG),
+])
+def test_fwd_fp8v_rejects_bad_arguments(L, kw, code):
+    assert fwd8(L, **kw) == code
+
+
+def test_fwd_fp8v_empty_problems_are_noops(L):
+    assert fwd8(L, B=0) == fa.FA_OK
+    assert fwd8(L, Nq=0, q=None, o=None, lse=None) == fa.FA_OK
+
+
 def test_fwd_empty_problems_are_noops(L):
     assert fwd(L, B=0) == fa.FA_OK
     assert fwd(L, H=0) == fa.FA_OK

@@ -148,6 +148,45 @@ fa_status fwd_impl(const Tensor4& q, const Tensor4& k, const Tensor4& v, const T
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+fa_status fwd_fp8v_impl(const void* q, const void* k, const void* vt, void* o, float* lse, int B, int H, int Nq,
+                        int Nk, int d, int64_t ld, float sm_scale, int causal, fa_dtype dtype, void* stream) {
+  fa_status st = check_common(B, H, Nq, Nk, d, sm_scale, causal, dtype);
+  if (st != FA_OK) return st;
+  if (d == 128) return FA_ERR_UNSUPPORTED;   // no TMEM columns for a separate P (see include/fa.h)
+  if (ld < Nk || ld % 16 != 0 || ld >= (int64_t(1) << 32)) return FA_ERR_INVALID_ARG;
+  if (B == 0 || H == 0 || Nq == 0) return FA_OK;
+  const Tensor4 tq = contiguous(q, H, Nq, d), tk = contiguous(k, H, Nk, d), to = contiguous(o, H, Nq, d);
+  if (!valid_tensor(tq) || !valid_tensor(tk) || !valid_tensor(to)) return FA_ERR_INVALID_ARG;
+  if (vt == nullptr || !aligned16(vt)) return FA_ERR_INVALID_ARG;
+  if (lse == nullptr || !aligned16(lse)) return FA_ERR_INVALID_ARG;
+  if (get_encode() == nullptr) return FA_ERR_CUDA;
+  cudaError_t e;
+  int* err = err_word(&e);
+  if (err == nullptr) return FA_ERR_CUDA;
+  FwdArgs a;
+  a.q = tq;
+  a.k = tk;
+  a.v.ptr = vt;
+  a.v.ss = ld;
+  a.v.sh = ld * d;
+  a.v.sb = ld * d * H;
+  a.o = to;
+  a.lse = lse;
+  a.B = B;
+  a.H = H;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.d = d;
+  a.sm_scale = sm_scale;
+  a.causal = causal;
+  a.bf16 = dtype == FA_BF16;
+  a.err = err;
+  a.fp8v = true;
+  a.vt_ld = ld;
+  e = launch_fwd(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 size_t ws_bytes(int B, int H, int Nq) {
   if (B <= 0 || H <= 0 || Nq <= 0) return 0;
   return 2 * sizeof(float) * static_cast<size_t>(B) * H * nq_pad(Nq);
@@ -218,6 +257,21 @@ bool make_tile_map(CUtensorMap* map, const Tensor4& t, int d, int rows, int H, i
   return r == CUDA_SUCCESS;
 }
 
+bool make_vt_map(CUtensorMap* map, const void* vt, int64_t ld, int Nk, int d, int H, int B) {
+  EncodeTiledFn enc = get_encode();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(Nk), static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(ld), static_cast<cuuint64_t>(ld * d),
+                                 static_cast<cuuint64_t>(ld * d * H)};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(kTileRows), static_cast<cuuint32_t>(d), 1, 1};
+  const cuuint32_t estride[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(vt), dims, strides, box, estride,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace fa
 
 using fa::Tensor4;
@@ -228,6 +282,11 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  int d, float sm_scale, int causal, fa_dtype dtype, void* stream) {
   return fa::fwd_impl(fa::contiguous(q, H, Nq, d), fa::contiguous(k, H, Nk, d), fa::contiguous(v, H, Nk, d),
                       fa::contiguous(o, H, Nq, d), lse, B, H, Nq, Nk, d, sm_scale, causal, dtype, stream);
+}
+
+fa_status fa_fwd_fp8v(const void* q, const void* k, const void* vt, void* o, float* lse, int B, int H, int Nq,
+                      int Nk, int d, int64_t vt_ld, float sm_scale, int causal, fa_dtype dtype, void* stream) {
+  return fa::fwd_fp8v_impl(q, k, vt, o, lse, B, H, Nq, Nk, d, vt_ld, sm_scale, causal, dtype, stream);
 }
 
 fa_status fa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,

@@ -187,6 +187,51 @@ __device__ __forceinline__ void issue_pv(uint32_t o_tmem, uint32_t p_tmem, uint3
     if (elect_one()) umma_ts(o_tmem, p_tmem + ks * 8, desc_add(bd0, ks * 16 * G::ROWB), idesc, (acc || ks > 0) ? 1u : 0u);
 }
 
+// O_t (+)= P V_j with P in e5m2, four per TMEM column (32 columns at p_tmem),
+// and V_j^T an e5m2 tile of D rows x 128 keys (K-major: 128-byte rows, the
+// 128-byte swizzle, 8-row groups 1024 bytes apart); K = 32 keys per MMA.
+template <int D>
+__device__ __forceinline__ void issue_pv_f8(uint32_t o_tmem, uint32_t p_tmem, uint32_t vt_addr, bool acc) {
+  constexpr uint32_t idesc = make_idesc_f8(kFmtE5M2, kFmtE5M2, kBM, D);
+  const uint64_t bd0 = make_sdesc(vt_addr, 16, 1024, 2);
+#pragma unroll
+  for (int ks = 0; ks < kBN / 32; ++ks)
+    if (elect_one()) umma_ts_f8(o_tmem, p_tmem + ks * 8, desc_add(bd0, ks * 32), idesc, (acc || ks > 0) ? 1u : 0u);
+}
+
+// p = exp2(c s - m) over the 128 scores of this thread's row (cs2 = (c, c),
+// nm2 = (-m, -m)), packed as the A operand of the PV product: two 16-bit
+// values per register, or four e5m2 values (FP8V: the cast of "Fused
+// Attention 2" before the product with V).  Returns the sum of the unrounded
+// p.
+template <bool BF16, bool FP8V>
+__device__ __forceinline__ float exp_pack(const float (&s)[kBN], uint64_t cs2, uint64_t nm2,
+                                          uint32_t (&pk)[FP8V ? kBN / 4 : kBN / 2]) {
+  uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+  float q0 = 0.f, q1 = 0.f;   // FP8V: the previous pair, waiting for its partner
+#pragma unroll
+  for (int e = 0; e < kBN / 2; ++e) {
+    float x0, x1;
+    f2unpack(ffma2(f2pack(s[2 * e], s[2 * e + 1]), cs2, nm2), x0, x1);
+    const float p0 = ex2_approx(x0);
+    const float p1 = ex2_approx(x1);
+    acc[e & 3] = fadd2(acc[e & 3], f2pack(p0, p1));
+    if constexpr (FP8V) {
+      if (e & 1) {
+        pk[e >> 1] = pack4_e5m2(q0, q1, p0, p1);
+      } else {
+        q0 = p0;
+        q1 = p1;
+      }
+    } else {
+      pk[e] = pack2<BF16>(p0, p1);
+    }
+  }
+  float a0, a1;
+  f2unpack(fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3])), a0, a1);
+  return a0 + a1;
+}
+
 template <int D, bool BF16>
 __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -575,7 +620,7 @@ struct FwdSpCfg {
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool FP8V>
 __global__ void __launch_bounds__(FwdSpCfg<D>::THREADS, 1)
     fwd_sp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -671,11 +716,17 @@ __global__ void __launch_bounds__(FwdSpCfg<D>::THREADS, 1)
           nfill = f;
           break;
         }
-        mbar_arrive_expect_tx(&bar_full[s], C::TILE);
-        const CUtensorMap* map = (f & 1) ? &tmV : &tmK;
-        for (int c = 0; c < C::G::NCH; ++c)
-          tma_load_4d(sKV + s * C::TILE + c * C::G::CHB, map, &bar_full[s], c * C::G::CC, (kt0 + (f >> 1)) * kBN,
-                      h, b);
+        if (FP8V && (f & 1)) {
+          // V_j^T: D rows of 128 keys, one box
+          mbar_arrive_expect_tx(&bar_full[s], D * kBN);
+          tma_load_4d(sKV + s * C::TILE, &tmV, &bar_full[s], (kt0 + (f >> 1)) * kBN, 0, h, b);
+        } else {
+          mbar_arrive_expect_tx(&bar_full[s], C::TILE);
+          const CUtensorMap* map = (f & 1) ? &tmV : &tmK;
+          for (int c = 0; c < C::G::NCH; ++c)
+            tma_load_4d(sKV + s * C::TILE + c * C::G::CHB, map, &bar_full[s], c * C::G::CC,
+                        (kt0 + (f >> 1)) * kBN, h, b);
+        }
       }
       for (int f = max(0, nfill - NS); f < nfill; ++f) mbar_wait_drain(&bar_full[f % NS], (f / NS) & 1);
 #pragma unroll
@@ -719,7 +770,10 @@ __global__ void __launch_bounds__(FwdSpCfg<D>::THREADS, 1)
         mbar_wait(bar_pready, k & 1, p.err, 5);
         __syncwarp();
         tc_fence_after();
-        issue_pv<D, BF16>(tmem + C::kColO + t * D, tmem + C::kColP, skv_addr + (f % NS) * C::TILE, j > 0);
+        if constexpr (FP8V)
+          issue_pv_f8<D>(tmem + C::kColO + t * D, tmem + C::kColP, skv_addr + (f % NS) * C::TILE, j > 0);
+        else
+          issue_pv<D, BF16>(tmem + C::kColO + t * D, tmem + C::kColP, skv_addr + (f % NS) * C::TILE, j > 0);
         if (elect_one()) {
           umma_commit(&bar_pv[t]);
           if (j == nkt[t] - 1) umma_commit(&bar_o[t]);
@@ -795,31 +849,19 @@ __global__ void __launch_bounds__(FwdSpCfg<D>::THREADS, 1)
         pj = j - 1;
       }
 
-      uint32_t pk[kBN / 2];
+      constexpr int NPK = FP8V ? kBN / 4 : kBN / 2;   // P registers (and TMEM columns) per row
+      uint32_t pk[NPK];
       bool done = false;
       if (j > 0) {
         // Common case: p = exp2(c s - m) against the running max m.  A row
         // sum <= 2^8 bounds every p of the row by 2^8, i.e. its max grew by
         // at most 8 and the exact path below would keep m: this P is its
         // result.
-        const uint64_t nm2 = f2pack(-m, -m);
-        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-        for (int e = 0; e < kBN / 2; ++e) {
-          float x0, x1;
-          f2unpack(ffma2(f2pack(s[2 * e], s[2 * e + 1]), cs2, nm2), x0, x1);
-          const float p0 = ex2_approx(x0);
-          const float p1 = ex2_approx(x1);
-          acc[e & 3] = fadd2(acc[e & 3], f2pack(p0, p1));
-          pk[e] = pack2<BF16>(p0, p1);
-        }
+        const float sum = exp_pack<BF16, FP8V>(s, cs2, f2pack(-m, -m), pk);
         // P complete before the wait for the buffer: the compiler may
         // otherwise sink its conversions past the wait.
-        tmem_reg_tie(*reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-        tmem_reg_tie(*reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-        float a0, a1;
-        f2unpack(fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3])), a0, a1);
-        const float sum = a0 + a1;
+#pragma unroll
+        for (int i = 0; i < NPK / 32; ++i) tmem_reg_tie(*reinterpret_cast<uint32_t(*)[32]>(&pk[32 * i]));
         if (!__any_sync(0xffffffffu, !(sum <= kFastSumBound))) {
           l += sum;
           done = true;
@@ -865,23 +907,10 @@ __global__ void __launch_bounds__(FwdSpCfg<D>::THREADS, 1)
           }
         }
         const float mb = (m == -CUDART_INF_F) ? 0.f : m;
-        const uint64_t nm2 = f2pack(-mb, -mb);
-        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-        for (int e = 0; e < kBN / 2; ++e) {
-          float x0, x1;
-          f2unpack(ffma2(f2pack(s[2 * e], s[2 * e + 1]), cs2, nm2), x0, x1);
-          const float p0 = ex2_approx(x0);
-          const float p1 = ex2_approx(x1);
-          acc[e & 3] = fadd2(acc[e & 3], f2pack(p0, p1));
-          pk[e] = pack2<BF16>(p0, p1);
-        }
-        float a0, a1;
-        f2unpack(fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3])), a0, a1);
-        l += a0 + a1;
+        l += exp_pack<BF16, FP8V>(s, cs2, f2pack(-mb, -mb), pk);
       }
 #pragma unroll
-      for (int i = 0; i < kBN / 32; ++i) tmem_st16(tP + i * 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[i * 16]));
+      for (int i = 0; i < NPK / 16; ++i) tmem_st16(tP + i * 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[i * 16]));
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -967,12 +996,13 @@ __global__ void __launch_bounds__(128) fwd_merge_kernel(const MergeParams mp) {
   if (lane == 0) mp.lse[static_cast<size_t>(bh) * mp.Nq + q] = wsum > 0.f ? mx + logf(wsum) : -CUDART_INF_F;
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool FP8V>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   using C = FwdCfg<D>;
   CUtensorMap tq, tk, tv;
-  if (!make_tile_map(&tq, a.q, D, a.Nq, a.H, a.B, BF16) || !make_tile_map(&tk, a.k, D, a.Nk, a.H, a.B, BF16) ||
-      !make_tile_map(&tv, a.v, D, a.Nk, a.H, a.B, BF16))
+  const bool v_ok = FP8V ? make_vt_map(&tv, a.v.ptr, a.vt_ld, a.Nk, D, a.H, a.B)
+                         : make_tile_map(&tv, a.v, D, a.Nk, a.H, a.B, BF16);
+  if (!make_tile_map(&tq, a.q, D, a.Nq, a.H, a.B, BF16) || !make_tile_map(&tk, a.k, D, a.Nk, a.H, a.B, BF16) || !v_ok)
     return cudaErrorInvalidValue;
   FwdParams p;
   p.B = a.B;
@@ -999,7 +1029,7 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   if constexpr (kSepP<D>) {
     using CS = FwdSpCfg<D>;
-    auto kern = fwd_sp_kernel<D, BF16>;
+    auto kern = fwd_sp_kernel<D, BF16, FP8V>;
     // setmaxnreg.inc waits until the block's launch registers cover the
     // split: never launch a build whose register count would not.
     static const int num_regs = [&] {
@@ -1011,6 +1041,8 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CS::SMEM);
     if (e != cudaSuccess) return e;
     kern<<<static_cast<unsigned>(blocks), CS::THREADS, CS::SMEM, stream>>>(tq, tk, tv, p);
+  } else if constexpr (FP8V) {
+    return cudaErrorInvalidValue;   // e5m2 V needs a P region of its own
   } else {
     auto kern = fwd_kernel<D, BF16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -1040,10 +1072,19 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
+  if (a.fp8v) {
+    if (a.n_splits > 1) return cudaErrorInvalidValue;
+    switch (a.d) {
+      case 64: return a.bf16 ? launch_fwd_t<64, true, true>(a, stream) : launch_fwd_t<64, false, true>(a, stream);
+      case 80: return a.bf16 ? launch_fwd_t<80, true, true>(a, stream) : launch_fwd_t<80, false, true>(a, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (a.d) {
-    case 64: return a.bf16 ? launch_fwd_t<64, true>(a, stream) : launch_fwd_t<64, false>(a, stream);
-    case 80: return a.bf16 ? launch_fwd_t<80, true>(a, stream) : launch_fwd_t<80, false>(a, stream);
-    case 128: return a.bf16 ? launch_fwd_t<128, true>(a, stream) : launch_fwd_t<128, false>(a, stream);
+    case 64: return a.bf16 ? launch_fwd_t<64, true, false>(a, stream) : launch_fwd_t<64, false, false>(a, stream);
+    case 80: return a.bf16 ? launch_fwd_t<80, true, false>(a, stream) : launch_fwd_t<80, false, false>(a, stream);
+    case 128:
+      return a.bf16 ? launch_fwd_t<128, true, false>(a, stream) : launch_fwd_t<128, false, false>(a, stream);
     default: return cudaErrorInvalidValue;
   }
 }

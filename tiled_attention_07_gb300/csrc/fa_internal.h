@@ -26,6 +26,11 @@ struct FwdArgs {
   // [n_splits][B*H][nq_pad(Nq)][d] and [n_splits][B*H][nq_pad(Nq)].
   int n_splits = 1;
   float* part = nullptr;
+  // V in float8 e5m2, transposed: v.ptr is [B][H][d][vt_ld] bytes (key j of
+  // head dim c at byte ((b H + h) d + c) vt_ld + j); P is cast to e5m2 for
+  // the PV product.
+  bool fp8v = false;
+  int64_t vt_ld = 0;
 };
 
 struct BwdArgs {
@@ -83,6 +88,9 @@ __host__ __device__ inline void chunked_order(int lin, int n_tiles, int BH, int*
 // Encodes a 4-D TMA map {d, rows, H, B} with a {chunk_cols(d), 128, 1, 1}
 // box and the matching swizzle.  Returns false if the driver rejects it.
 bool make_tile_map(CUtensorMap* map, const Tensor4& t, int d, int rows, int H, int B, bool bf16);
+// Tensor map of a transposed e5m2 V: boxes of 128 keys (one 128-byte row,
+// 128-byte swizzle) by d rows.
+bool make_vt_map(CUtensorMap* map, const void* vt, int64_t ld, int Nk, int d, int H, int B);
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 // phase: 0 = all three launches; 1 = D / log2-LSE preprocess; 2 = dK, dV;

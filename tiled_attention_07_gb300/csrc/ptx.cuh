@@ -216,6 +216,16 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       : "memory");
 }
 
+// kind::f8f6f4 (8-bit operands, f32 accumulate), A from tensor memory.
+__device__ __forceinline__ void umma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred P;\n setp.ne.u32 P, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, P;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive (once) on `bar` when every tcgen05.mma issued so far by this thread
 // has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
@@ -231,6 +241,14 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 __host__ __device__ constexpr uint32_t make_idesc_f16(bool bf16, int M, int N, bool a_mn_major, bool b_mn_major) {
   return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) | ((a_mn_major ? 1u : 0u) << 15) |
          ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Instruction descriptor of kind::f8f6f4 with f32 accumulation, both
+// operands K-major: the same fields as above, with the operand formats
+// 0 = e4m3, 1 = e5m2 in bits 7-9 (A) and 10-12 (B).
+constexpr uint32_t kFmtE5M2 = 1;
+__host__ __device__ constexpr uint32_t make_idesc_f8(uint32_t a_fmt, uint32_t b_fmt, int M, int N) {
+  return (1u << 4) | (a_fmt << 7) | (b_fmt << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // Shared-memory matrix descriptor of a swizzled tile (the layouts TMA writes
@@ -412,6 +430,19 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   } else {
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   }
+  return r;
+}
+
+// Four floats to e5m2 (round to nearest even, saturating to +-57344), a in
+// the lowest byte: the order of consecutive K elements in an 8-bit operand.
+__device__ __forceinline__ uint32_t pack4_e5m2(float a, float b, float c, float d) {
+  uint32_t r;
+  asm("{\n .reg .b16 lo, hi;\n"
+      " cvt.rn.satfinite.e5m2x2.f32 lo, %2, %1;\n"
+      " cvt.rn.satfinite.e5m2x2.f32 hi, %4, %3;\n"
+      " mov.b32 %0, {lo, hi};\n}\n"
+      : "=r"(r)
+      : "f"(a), "f"(b), "f"(c), "f"(d));
   return r;
 }
 

@@ -52,6 +52,7 @@ EXPORTED_SYMBOLS = (
     "fa_fwd_split_workspace_bytes",
     "fa_fwd_split_count",
     "fa_fwd_split",
+    "fa_fwd_fp8v",
     "fa_bwd_workspace_bytes",
     "fa_bwd",
     "fa_bwd_strided",
@@ -107,6 +108,8 @@ def lib() -> ctypes.CDLL:
         L.fa_fwd_split.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, ctypes.POINTER(Layout), i, vp,
                                    ctypes.c_size_t, vp]
         L.fa_fwd_split.restype = i
+        L.fa_fwd_fp8v.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.c_int64, f, i, i, vp]
+        L.fa_fwd_fp8v.restype = i
         L.fa_bwd_workspace_bytes.argtypes = [i, i, i, i, i]
         L.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
         L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, ctypes.c_size_t, vp]
@@ -210,6 +213,34 @@ def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, l
                               int(bool(causal)), dt, ctypes.byref(lay), _stream(stream))
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd")
+
+
+def fa_fwd_fp8v(q: torch.Tensor, k: torch.Tensor, vt: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
+                sm_scale: float, causal: bool, stream=None) -> None:
+    """The forward with V in float8 e5m2, transposed: ``vt`` is [B, H, d, ld]
+    (torch.float8_e5m2 or its raw uint8 codes) with unit stride along keys,
+    ld = vt.stride(2) >= Nk and a multiple of 16; q, k, o contiguous
+    [B, H, seq, d] fp16/bf16."""
+    _check_cuda(q, k, vt, o, lse)
+    B, H, Nq, d = _dims(q)
+    _, _, Nk, _ = _dims(k)
+    dt = _dtype_code(q)
+    if vt.dtype not in (torch.float8_e5m2, torch.uint8):
+        raise TypeError(f"vt must be float8_e5m2 (or its uint8 codes), got {vt.dtype}")
+    if vt.dim() != 4 or tuple(vt.shape[:3]) != (B, H, d) or vt.shape[3] < Nk or vt.stride(3) != 1:
+        raise ValueError(f"vt must be [B, H, d, >= Nk] with unit key stride, got {tuple(vt.shape)}")
+    ld = vt.stride(2)
+    if vt.stride(1) != d * ld or vt.stride(0) != H * d * ld:
+        raise ValueError("vt rows must be packed: strides (H*d*ld, d*ld, ld, 1)")
+    if lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 tensor [B, H, Nq]")
+    for t in (q, k, o):
+        if not _is_bhsd_contiguous(t):
+            raise ValueError("q, k and o must be contiguous [B, H, seq, d]")
+    rc = lib().fa_fwd_fp8v(_ptr(q), _ptr(k), _ptr(vt), _ptr(o), _ptr(lse), B, H, Nq, Nk, d, int(ld),
+                           float(sm_scale), int(bool(causal)), dt, _stream(stream))
+    if rc != FA_OK:
+        raise FaError(rc, "fa_fwd_fp8v")
 
 
 def fa_fwd_split_workspace_bytes(B: int, H: int, Nq: int, d: int, n_splits: int) -> int:

@@ -137,6 +137,27 @@ def make_inputs(w: Workload, device: str = "cpu", with_grad_output: Optional[boo
     return out
 
 
+def fp8v_inputs(w: Workload, device: str = "cpu", ld: Optional[int] = None, pad_code: int = 0) -> Dict[str, torch.Tensor]:
+    """q, k of ``make_inputs`` and its V stored for the e5m2 path: transposed
+    to ``[B, H, d, Nk]``, cast to float8 e5m2 by torch (round to nearest even)
+    and held as raw codes (uint8) in rows of ``ld`` bytes (default Nk rounded
+    up to 16), the bytes past Nk set to ``pad_code``.  Returns q, k, ``vt``
+    (uint8 [B, H, d, ld]) and ``v8`` (the same V values, float32 [B, H, Nk, d])."""
+    if w.layout != "bhsd":
+        raise ValueError("the e5m2 V path takes the [B, H, seq, d] layout")
+    x = make_inputs(w, "cpu", with_grad_output=False)
+    if ld is None:
+        ld = (w.Nk + 15) // 16 * 16
+    codes = x["v"].float().transpose(-1, -2).contiguous().to(torch.float8_e5m2).view(torch.uint8)
+    vt = torch.full((w.B, w.H, w.d, ld), pad_code, dtype=torch.uint8)
+    vt[..., : w.Nk] = codes
+    out = {"q": x["q"], "k": x["k"], "vt": vt,
+           "v8": codes.view(torch.float8_e5m2).float().transpose(-1, -2).contiguous()}
+    if device != "cpu":
+        out = {k: t.to(device) for k, t in out.items()}
+    return out
+
+
 def head_view(t: torch.Tensor, layout: str, b: int, h: int) -> torch.Tensor:
     """The ``[seq, d]`` matrix of one (batch, head) pair."""
     if layout == "bhsd":
