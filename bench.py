@@ -51,6 +51,8 @@ def parse_args(argv=None):
     ap.add_argument("--fwd-only", action="store_true",
                     help="time only the forward of --workload (the forward-only configurations), one JSON line")
     ap.add_argument("--split", default="1", help="with --fwd-only: key-range splits (an integer, or 'auto')")
+    ap.add_argument("--fp8v", action="store_true",
+                    help="with --fwd-only: V in float8 e5m2, transposed, P cast to e5m2 (fa_fwd_fp8v)")
     ap.add_argument("--softmax", default=None, metavar="WORKLOAD",
                     help="time the row-softmax kernel on a named softmax workload instead, one JSON line")
     ap.add_argument("--source-hash", default=None, metavar="KERNEL",
@@ -339,13 +341,19 @@ def run_fwd_only(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = pick_workload(args)
-    x = {k: t.to(dev) for k, t in W.make_inputs(w, device="cpu", with_grad_output=False).items()}
-    q, k, v = x["q"], x["k"], x["v"]
+    if args.fp8v:
+        x = {k: t.to(dev) for k, t in W.fp8v_inputs(w, device="cpu").items() if k != "v8"}
+        q, k, v = x["q"], x["k"], x["vt"]
+    else:
+        x = {k: t.to(dev) for k, t in W.make_inputs(w, device="cpu", with_grad_output=False).items()}
+        q, k, v = x["q"], x["k"], x["v"]
     o = torch.empty_like(q)
     lse = torch.empty(fa.lse_shape(q), dtype=torch.float32, device=dev)
     B, H, Nq, d = fa._dims(q)
     Nk = fa._dims(k)[2]
     n_splits = fa.fa_fwd_split_count(B, H, Nq, Nk, d, w.causal) if args.split == "auto" else int(args.split)
+    if args.fp8v and n_splits != 1:
+        raise SystemExit("--fp8v runs unsplit")
     nbytes = fa.fa_fwd_split_workspace_bytes(B, H, Nq, d, n_splits)
     ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -353,7 +361,9 @@ def run_fwd_only(args):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if in_bytes < (256 << 20) else None
 
     def fwd():
-        if n_splits > 1:
+        if args.fp8v:
+            fa.fa_fwd_fp8v(q, k, v, o, lse, w.sm_scale, w.causal, stream)
+        elif n_splits > 1:
             fa.fa_fwd_split(q, k, v, o, lse, w.sm_scale, w.causal, n_splits, ws, stream)
         else:
             fa.fa_fwd(q, k, v, o, lse, w.sm_scale, w.causal, stream)
@@ -390,19 +400,26 @@ def run_fwd_only(args):
     value = world * flops / (ms_step / 1e3) / 1e12
     peaks, peak_src = load_peaks()
     peak = peaks["bf16_tflops"]
+    peak_note = f"{peak_src} bf16 burst (kernel timed alone)"
+    if args.fp8v:
+        # Half the FLOPs (S = q k^T) at the 16-bit rate P, half (P V) at the
+        # 8-bit rate, taken as 2 P (the nominal fp8 : bf16 ratio): time at
+        # peak F/2 (1/P + 1/(2P)), i.e. an effective peak of 4P/3.
+        peak = round(peak * 4.0 / 3.0, 1)
+        peak_note = f"{peak_src} bf16 burst x 4/3: S at the 16-bit rate, PV at 2x (nominal fp8:bf16 ratio)"
     line = {
         "metric": "attention forward TFLOP/s on 1 GB300 (forward-only configuration)", "value": round(value, 2),
         "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": max(args.warmup, 3),
         "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": w.dtype, "data": "synthetic (seeded q, k, v)",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": w.causal,
-                   "layout": w.layout, "split": n_splits, "flops_per_step": flops,
+        "dtype": (w.dtype + " q,k,o; e5m2 v,p") if args.fp8v else w.dtype, "data": "synthetic (seeded q, k, v)",
+        "config": {"workload": w.name + ("_fp8v" if args.fp8v else ""), "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk,
+                   "d": w.d, "causal": w.causal, "layout": w.layout, "split": n_splits, "flops_per_step": flops,
                    "l2": "256 MB scratch write between steps" if flush is not None else "inputs larger than L2",
                    "parallelism": f"replica x{world}"},
         "roofline": {"bound": "tensor", "kernel": "fwd" + ("+merge" if n_splits > 1 else ""),
                      "achieved": round(value / world, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(value / world / peak, 4), "traffic": None,
-                     "peak_source": f"{peak_src} bf16 burst (kernel timed alone)"},
+                     "peak_source": peak_note},
         "clocks": clk, "gpu_launches": K * (2 if n_splits > 1 else 1), "e2e": None, "cpu_baseline": None,
     }
     if rank == 0:

@@ -86,6 +86,36 @@ def test_edge_cases(case):
     check(w, guard=1024)
 
 
+# Shapes with enough heads that the separate-P forward (d <= 96) runs blocks
+# that walk several work units (two query-tile pairs of one head each, the
+# heaviest with the lightest) plus one-item blocks for the rest: two or more
+# rounds of units per SM on a 152-SM part.
+PERSIST = [
+    # dtype, layout, B, H, Nq, Nk, d, causal
+    ("bf16", "bhsd", 2, 160, 512, 512, 80, True),    # one pair per unit side, 320 units
+    ("fp16", "bhsd", 1, 200, 768, 768, 64, True),    # three pairs: the middle pair alone in its unit
+    ("bf16", "bhsd", 1, 256, 700, 700, 80, False),   # ragged Nq whose last pair still has rows in tile 1
+    ("bf16", "bhsd", 1, 320, 1024, 1500, 64, True),  # causal with Nq < Nk
+]
+
+
+@pytest.mark.parametrize("case", PERSIST, ids=["-".join(map(str, c)) for c in PERSIST])
+def test_persistent_units(case):
+    dt, layout, B, H, Nq, Nk, d, causal = case
+    w = W.custom(dt, layout, B, H, Nq, Nk, d, causal, std=0.5 if dt == "fp16" else 1.0, seed=Nq + H)
+    x = W.make_inputs(w, device="cuda")
+    o, lse = run_fwd(w, x, guard=1024)
+    stats = {}
+    heads = [(b, h) for b in range(B) for h in range(H)]
+    for b, h in heads[:2] + heads[len(heads) // 2:len(heads) // 2 + 2] + heads[-2:]:
+        check_fwd_head(w, x, o, lse, b, h, stats)
+    # every head was written (NaN-free) and equals a second, identical run
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    o2, lse2 = run_fwd(w, x)
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    print(w.name, stats)
+
+
 def test_large_logits_trigger_rescaling():
     # q, k spread widely so that running maxima jump by more than 2^8 between
     # key tiles (checks the lazy O rescaling); v stays N(0, 1) so that |O|

@@ -83,6 +83,11 @@ struct FwdParams {
   int Nqp;              // query rows padded to whole tiles (partial buffers)
   float* part_o;        // [n_splits][B*H][Nqp][d]
   float* part_lse;      // [n_splits][B*H][Nqp]
+  // Work split of the separate-P forward (n_splits == 1 only): blocks
+  // [0, grid_p) each walk units b, b + grid_p, ... below persist_units; the
+  // other blocks take one item each of the remaining units (see sp_next).
+  int grid_p = 0;
+  int persist_units = 0;
 };
 
 // Number of key tiles query tile t (rows r0 .. r0+127) needs.
@@ -596,13 +601,85 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 template <int D>
 constexpr bool kSepP = 256 + 2 * D + 64 <= 512;
 
+// One work item of the separate-P forward: the key tiles of split `split` for
+// the query-tile pair of rank `rank` (0 = the heaviest) of head bh.  An item
+// with n_max == 0 has no work.
+struct SpItem {
+  int b, h, bh, split, q0, kt0, n_max;
+  int nkt[kNQT];   // key tiles of query tile t: [kt0, kt0 + nkt[t])
+};
+
+__device__ __forceinline__ SpItem sp_item(const FwdParams& p, int rank, int bh, int split) {
+  SpItem it;
+  it.split = split;
+  it.bh = bh;
+  const int pair = p.n_pairs - 1 - rank;
+  it.b = bh / p.H;
+  it.h = bh % p.H;
+  it.q0 = pair * (kNQT * kBM);
+  it.kt0 = split * p.tiles_per_split;
+  it.n_max = 0;
+#pragma unroll
+  for (int t = 0; t < kNQT; ++t) {
+    it.nkt[t] = max(0, min(key_tiles(it.q0 + t * kBM, p.Nq, p.Nk, p.causal), it.kt0 + p.tiles_per_split) - it.kt0);
+    it.n_max = max(it.n_max, it.nkt[t]);
+  }
+  return it;
+}
+
+// The q-th work item of this block; false past its last one.
+// Without persistent blocks (grid_p == 0) block w takes the single item w:
+// split w % n_splits of the pair of rank w / n_splits in chunked_order.
+// Otherwise the work is cut into units: unit u of head bh holds the pairs of
+// ranks r and n_pairs - 1 - r (the heaviest with the lightest, so that under
+// the causal mask every unit has the same number of key tiles; an odd middle
+// pair is alone), units in chunked_order.  Block b < grid_p walks the units
+// b, b + grid_p, ... below persist_units, two items each; each later block
+// takes one item of the remaining units, first items (heavy) in unit order,
+// then second items (light) in reverse, so that the hardware hands the
+// leftover work out heaviest first.
+__device__ __forceinline__ bool sp_next(const FwdParams& p, int q, SpItem* it) {
+  const int BH = p.B * p.H;
+  const int bid = static_cast<int>(blockIdx.x);
+  int r, bh;
+  if (p.grid_p == 0) {
+    if (q > 0) return false;
+    chunked_order(bid / p.n_splits, p.n_pairs, BH, &r, &bh);
+    *it = sp_item(p, r, bh, bid % p.n_splits);
+    return true;
+  }
+  const int units = (p.n_pairs + 1) / 2;
+  int u, second;
+  if (bid < p.grid_p) {
+    u = bid + (q >> 1) * p.grid_p;
+    if (u >= p.persist_units) return false;
+    second = q & 1;
+  } else {
+    if (q > 0) return false;
+    const int n_tail = units * BH - p.persist_units;
+    const int ti = bid - p.grid_p;
+    second = ti >= n_tail ? 1 : 0;
+    u = p.persist_units + (second ? 2 * n_tail - 1 - ti : ti);
+  }
+  chunked_order(u, units, BH, &r, &bh);
+  const int rank = second ? p.n_pairs - 1 - r : r;
+  if (second && rank == r) {   // the odd middle pair: no second item
+    it->n_max = 0;
+    it->nkt[0] = it->nkt[1] = 0;
+    it->b = it->h = it->bh = it->split = it->q0 = it->kt0 = 0;
+    return true;
+  }
+  *it = sp_item(p, rank, bh, 0);
+  return true;
+}
+
 template <int D>
 struct FwdSpCfg {
   using G = TileGeo<D>;
   static constexpr int TILE = G::TILE;
   static constexpr int NSTAGE = D == 64 ? 8 : 6;   // even: K_j in even slots, V_j in odd
   static constexpr int SMEM_DATA = kNQT * TILE + NSTAGE * TILE;
-  static constexpr int NBARS = kNQT + 2 * NSTAGE + 4 * kNQT + 2;
+  static constexpr int NBARS = 2 * kNQT + 2 * NSTAGE + 4 * kNQT + 3;
   static constexpr int SMEM = 1024 + SMEM_DATA + NBARS * 8 + 16;
   static constexpr int THREADS = 384;
   static constexpr int PROD_WARP = 8;
@@ -632,41 +709,25 @@ __global__ void __launch_bounds__(FwdSpCfg<D>::THREADS, 1)
   uint8_t* sKV = smem + kNQT * C::TILE;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + NS * C::TILE);
   uint64_t* bar_q = bars;                      // [kNQT] Q_t landed
-  uint64_t* bar_full = bar_q + kNQT;           // [NS]
+  uint64_t* bar_qfree = bar_q + kNQT;          // [kNQT] last S_t of an item complete: Q_t may be replaced
+  uint64_t* bar_full = bar_qfree + kNQT;       // [NS]
   uint64_t* bar_empty = bar_full + NS;         // [NS] one release by the issuer that read the slot
   uint64_t* bar_s = bar_empty + NS;            // [kNQT] S_t,j complete
   uint64_t* bar_sfree = bar_s + kNQT;          // [kNQT] S_t,j in registers (one arrival per warp)
   uint64_t* bar_o = bar_sfree + kNQT;          // [kNQT] last PV of tile t complete
   uint64_t* bar_pv = bar_o + kNQT;             // [kNQT] PV_t,j complete (phase j)
   uint64_t* bar_pready = bar_pv + kNQT;        // next P write done (one arrival per warp of the writer)
-  uint64_t* bar_drain = bar_pready + 1;        // every MMA of both issuers complete
+  uint64_t* bar_item = bar_pready + 1;         // every PV of an item (with work) complete
+  uint64_t* bar_drain = bar_item + 1;          // every MMA of both issuers complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_drain + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  const int BH = p.B * p.H;
-  const int split = static_cast<int>(blockIdx.x) % p.n_splits;
-  int rank, bh;
-  chunked_order(static_cast<int>(blockIdx.x) / p.n_splits, p.n_pairs, BH, &rank, &bh);
-  const int pair = p.n_pairs - 1 - rank;
-  const int b = bh / p.H;
-  const int h = bh % p.H;
-  const int q0 = pair * (kNQT * kBM);
-  const int kt0 = split * p.tiles_per_split;   // first key tile of this block
-
-  // Key tiles of query tile t in this block: [kt0, kt0 + nkt[t]).
-  int nkt[kNQT];
-  int n_max = 0;
-#pragma unroll
-  for (int t = 0; t < kNQT; ++t) {
-    nkt[t] = max(0, min(key_tiles(q0 + t * kBM, p.Nq, p.Nk, p.causal), kt0 + p.tiles_per_split) - kt0);
-    n_max = max(n_max, nkt[t]);
-  }
-
   if (threadIdx.x == 0) {
     for (int t = 0; t < kNQT; ++t) {
       mbar_init(&bar_q[t], 1);
+      mbar_init(&bar_qfree[t], 1);
       mbar_init(&bar_s[t], 1);
       mbar_init(&bar_sfree[t], 4);
       mbar_init(&bar_o[t], 1);
@@ -677,6 +738,7 @@ __global__ void __launch_bounds__(FwdSpCfg<D>::THREADS, 1)
       mbar_init(&bar_empty[s], 1);
     }
     mbar_init(bar_pready, 4);
+    mbar_init(bar_item, 1);
     mbar_init(bar_drain, 2);
     fence_mbar_init();
   }
@@ -696,63 +758,89 @@ __global__ void __launch_bounds__(FwdSpCfg<D>::THREADS, 1)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
+      // Fill g (counted over all items of the block) of slot g % NS: fill
+      // 2 j of an item holds its K_j, fill 2 j + 1 its V_j.  A slot is
+      // refilled only after its previous fill has landed, so each slot has
+      // at most one copy in flight; a give-up stops the fills and only the
+      // fills issued are drained.
+      int F = 0;                  // fills issued
+      int qn[kNQT] = {0, 0};      // Q_t loads issued
+      bool stop = false;
+      for (int r = 0; !stop; ++r) {
+        SpItem it;
+        if (!sp_next(p, r, &it)) break;
 #pragma unroll
-      for (int t = 0; t < kNQT; ++t) {
-        if (nkt[t] == 0) continue;
-        mbar_arrive_expect_tx(&bar_q[t], C::TILE);
-        for (int c = 0; c < C::G::NCH; ++c)
-          tma_load_4d(sQ + t * C::TILE + c * C::G::CHB, &tmQ, &bar_q[t], c * C::G::CC, q0 + t * kBM, h, b);
-      }
-      // Fill f = 2 j holds K_j, f = 2 j + 1 holds V_j.  A slot is refilled
-      // only after its previous fill has landed, so each slot has at most one
-      // copy in flight; a give-up stops the fills and only the fills issued
-      // are drained.
-      int nfill = 2 * n_max;
-      for (int f = 0; f < nfill; ++f) {
-        const int s = f % NS;
-        const int use = f / NS;
-        if (use > 0 && (!mbar_wait(&bar_empty[s], (use - 1) & 1, p.err, 1) ||
-                        !mbar_wait_drain(&bar_full[s], (use - 1) & 1))) {
-          nfill = f;
-          break;
-        }
-        if (FP8V && (f & 1)) {
-          // V_j^T: D rows of 128 keys, one box
-          mbar_arrive_expect_tx(&bar_full[s], D * kBN);
-          tma_load_4d(sKV + s * C::TILE, &tmV, &bar_full[s], (kt0 + (f >> 1)) * kBN, 0, h, b);
-        } else {
-          mbar_arrive_expect_tx(&bar_full[s], C::TILE);
-          const CUtensorMap* map = (f & 1) ? &tmV : &tmK;
+        for (int t = 0; t < kNQT; ++t) {
+          if (it.nkt[t] == 0 || stop) continue;
+          // Q_t of the previous item is no longer read by its S MMAs.
+          if (qn[t] > 0 && !mbar_wait(&bar_qfree[t], (qn[t] - 1) & 1, p.err, 14)) {
+            stop = true;
+            continue;
+          }
+          mbar_arrive_expect_tx(&bar_q[t], C::TILE);
           for (int c = 0; c < C::G::NCH; ++c)
-            tma_load_4d(sKV + s * C::TILE + c * C::G::CHB, map, &bar_full[s], c * C::G::CC,
-                        (kt0 + (f >> 1)) * kBN, h, b);
+            tma_load_4d(sQ + t * C::TILE + c * C::G::CHB, &tmQ, &bar_q[t], c * C::G::CC, it.q0 + t * kBM, it.h, it.b);
+          ++qn[t];
+        }
+        for (int f = 0; f < 2 * it.n_max && !stop; ++f) {
+          const int g = F;
+          const int s = g % NS;
+          const int use = g / NS;
+          if (use > 0 && (!mbar_wait(&bar_empty[s], (use - 1) & 1, p.err, 1) ||
+                          !mbar_wait_drain(&bar_full[s], (use - 1) & 1))) {
+            stop = true;
+            break;
+          }
+          const int kt = it.kt0 + (f >> 1);
+          if (FP8V && (f & 1)) {
+            // V_j^T: D rows of 128 keys, one box
+            mbar_arrive_expect_tx(&bar_full[s], D * kBN);
+            tma_load_4d(sKV + s * C::TILE, &tmV, &bar_full[s], kt * kBN, 0, it.h, it.b);
+          } else {
+            mbar_arrive_expect_tx(&bar_full[s], C::TILE);
+            const CUtensorMap* map = (f & 1) ? &tmV : &tmK;
+            for (int c = 0; c < C::G::NCH; ++c)
+              tma_load_4d(sKV + s * C::TILE + c * C::G::CHB, map, &bar_full[s], c * C::G::CC, kt * kBN, it.h, it.b);
+          }
+          ++F;
         }
       }
-      for (int f = max(0, nfill - NS); f < nfill; ++f) mbar_wait_drain(&bar_full[f % NS], (f / NS) & 1);
+      for (int g = max(0, F - NS); g < F; ++g) mbar_wait_drain(&bar_full[g % NS], (g / NS) & 1);
 #pragma unroll
       for (int t = 0; t < kNQT; ++t)
-        if (nkt[t] > 0) mbar_wait_drain(&bar_q[t], 0);
+        if (qn[t] > 0) mbar_wait_drain(&bar_q[t], (qn[t] - 1) & 1);
    } else if (warp == C::MMA_WARP) {
     // ------------------------------------------------------ issuer A: S MMAs
     const uint32_t sq_addr = smem_u32(sQ);
     const uint32_t skv_addr = smem_u32(sKV);
-    for (int j = 0; j < n_max; ++j) {
-      const int f = 2 * j;
-      mbar_wait(&bar_full[f % NS], (f / NS) & 1, p.err, 3);
+    int F = 0;                  // fills of the items before this one
+    int sc[kNQT] = {0, 0};      // S_t issued
+    int qn[kNQT] = {0, 0};      // items before this one that had tile t
+    for (int r = 0;; ++r) {
+      SpItem it;
+      if (!sp_next(p, r, &it)) break;
+      for (int j = 0; j < it.n_max; ++j) {
+        const int g = F + 2 * j;
+        mbar_wait(&bar_full[g % NS], (g / NS) & 1, p.err, 3);
 #pragma unroll
-      for (int t = 0; t < kNQT; ++t) {
-        if (j >= nkt[t]) continue;
-        if (j == 0) {
-          mbar_wait(&bar_q[t], 0, p.err, 2);
-        } else {
-          mbar_wait(&bar_sfree[t], (j - 1) & 1, p.err, 13);   // S_t,j-1 read
+        for (int t = 0; t < kNQT; ++t) {
+          if (j >= it.nkt[t]) continue;
+          if (j == 0) mbar_wait(&bar_q[t], qn[t] & 1, p.err, 2);
+          if (sc[t] > 0) mbar_wait(&bar_sfree[t], (sc[t] - 1) & 1, p.err, 13);   // S_t before this one read
+          __syncwarp();
+          tc_fence_after();
+          issue_s<D, BF16>(tmem + t * 128, sq_addr + t * C::TILE, skv_addr + (g % NS) * C::TILE);
+          if (elect_one()) {
+            umma_commit(&bar_s[t]);
+            if (j == it.nkt[t] - 1) umma_commit(&bar_qfree[t]);   // last S_t of the item: Q_t free
+          }
+          ++sc[t];
         }
-        __syncwarp();
-        tc_fence_after();
-        issue_s<D, BF16>(tmem + t * 128, sq_addr + t * C::TILE, skv_addr + (f % NS) * C::TILE);
-        if (elect_one()) umma_commit(&bar_s[t]);
+        if (elect_one()) umma_commit(&bar_empty[g % NS]);   // K_j read by every S of step j
       }
-      if (elect_one()) umma_commit(&bar_empty[f % NS]);   // K_j read by every S of step j
+      F += 2 * it.n_max;
+#pragma unroll
+      for (int t = 0; t < kNQT; ++t) qn[t] += it.nkt[t] > 0 ? 1 : 0;
     }
     if (elect_one()) umma_commit(bar_drain);
     __syncwarp();
@@ -760,27 +848,34 @@ __global__ void __launch_bounds__(FwdSpCfg<D>::THREADS, 1)
    } else if (warp == C::MMA_WARP + 1) {
     // ----------------------------------------------------- issuer B: PV MMAs
     const uint32_t skv_addr = smem_u32(sKV);
+    int F = 0;   // fills of the items before this one
     int k = 0;   // number of the next P write
-    for (int j = 0; j < n_max; ++j) {
-      const int f = 2 * j + 1;
-      mbar_wait(&bar_full[f % NS], (f / NS) & 1, p.err, 4);
+    for (int r = 0;; ++r) {
+      SpItem it;
+      if (!sp_next(p, r, &it)) break;
+      for (int j = 0; j < it.n_max; ++j) {
+        const int g = F + 2 * j + 1;
+        mbar_wait(&bar_full[g % NS], (g / NS) & 1, p.err, 4);
 #pragma unroll
-      for (int t = 0; t < kNQT; ++t) {
-        if (j >= nkt[t]) continue;
-        mbar_wait(bar_pready, k & 1, p.err, 5);
-        __syncwarp();
-        tc_fence_after();
-        if constexpr (FP8V)
-          issue_pv_f8<D>(tmem + C::kColO + t * D, tmem + C::kColP, skv_addr + (f % NS) * C::TILE, j > 0);
-        else
-          issue_pv<D, BF16>(tmem + C::kColO + t * D, tmem + C::kColP, skv_addr + (f % NS) * C::TILE, j > 0);
-        if (elect_one()) {
-          umma_commit(&bar_pv[t]);
-          if (j == nkt[t] - 1) umma_commit(&bar_o[t]);
+        for (int t = 0; t < kNQT; ++t) {
+          if (j >= it.nkt[t]) continue;
+          mbar_wait(bar_pready, k & 1, p.err, 5);
+          __syncwarp();
+          tc_fence_after();
+          if constexpr (FP8V)
+            issue_pv_f8<D>(tmem + C::kColO + t * D, tmem + C::kColP, skv_addr + (g % NS) * C::TILE, j > 0);
+          else
+            issue_pv<D, BF16>(tmem + C::kColO + t * D, tmem + C::kColP, skv_addr + (g % NS) * C::TILE, j > 0);
+          if (elect_one()) {
+            umma_commit(&bar_pv[t]);
+            if (j == it.nkt[t] - 1) umma_commit(&bar_o[t]);
+          }
+          ++k;
         }
-        ++k;
+        if (elect_one()) umma_commit(&bar_empty[g % NS]);   // V_j read by every PV of step j
       }
-      if (elect_one()) umma_commit(&bar_empty[f % NS]);   // V_j read by every PV of step j
+      if (it.n_max > 0 && elect_one()) umma_commit(bar_item);
+      F += 2 * it.n_max;
     }
     if (elect_one()) umma_commit(bar_drain);
     __syncwarp();
@@ -792,141 +887,165 @@ __global__ void __launch_bounds__(FwdSpCfg<D>::THREADS, 1)
     const int t = warp >> 2;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
-    const int r0 = q0 + t * kBM;
-    const int qrow = r0 + row;
-    const int n = nkt[t];
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t tS = tmem + lane_off + t * 128;
     const uint32_t tO = tmem + lane_off + C::kColO + t * D;
     const uint32_t tP = tmem + lane_off + C::kColP;
     const float cs = p.scale_log2;
     const uint64_t cs2 = f2pack(cs, cs);
+    int sc = 0;                 // S_t read (phase of bar_s[t])
+    int on = 0;                 // items before this one with keys for tile t (phase of bar_o[t])
+    int pvb[kNQT] = {0, 0};     // PVs of each tile in the items before this one
+    int ni = 0;                 // items before this one with work (phase of bar_item)
 
-    float m = -CUDART_INF_F;  // running max of the scaled scores (log2 domain)
-    float l = 0.f;            // running sum of exp2(score - m)
+    for (int r = 0;; ++r) {
+      SpItem it;
+      if (!sp_next(p, r, &it)) break;
+      const int r0 = it.q0 + t * kBM;
+      const int qrow = r0 + row;
+      const int n = it.nkt[t];
 
-    for (int j = 0; j < n; ++j) {
-      mbar_wait(&bar_s[t], j & 1, p.err, 8);
-      tc_fence_after();
-      float s[kBN];
-      {
-        uint32_t r0_[32], r1_[32], r2_[32], r3_[32];
-        tmem_ld32(tS, r0_);
-        tmem_ld32(tS + 32, r1_);
-        tmem_ld32(tS + 64, r2_);
-        tmem_ld32(tS + 96, r3_);
-        tmem_wait_ld(r3_);
-        tmem_reg_tie(r0_);
-        tmem_reg_tie(r1_);
-        tmem_reg_tie(r2_);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          s[e] = __uint_as_float(r0_[e]);
-          s[32 + e] = __uint_as_float(r1_[e]);
-          s[64 + e] = __uint_as_float(r2_[e]);
-          s[96 + e] = __uint_as_float(r3_[e]);
-        }
-      }
-      // S_t,j is in registers: the tensor cores may overwrite it with S_t,j+1.
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_sfree[t]);
+      float m = -CUDART_INF_F;  // running max of the scaled scores (log2 domain)
+      float l = 0.f;            // running sum of exp2(score - m)
 
-      const int kbase = (kt0 + j) * kBN;
-      if (kbase + kBN > p.Nk || (p.causal && kbase + kBN - 1 > r0)) {
-        const int lim = p.causal ? min(p.Nk, qrow + 1) : p.Nk;  // keys < lim are visible
+      for (int j = 0; j < n; ++j) {
+        mbar_wait(&bar_s[t], sc & 1, p.err, 8);
+        ++sc;
+        tc_fence_after();
+        float s[kBN];
+        {
+          uint32_t r0_[32], r1_[32], r2_[32], r3_[32];
+          tmem_ld32(tS, r0_);
+          tmem_ld32(tS + 32, r1_);
+          tmem_ld32(tS + 64, r2_);
+          tmem_ld32(tS + 96, r3_);
+          tmem_wait_ld(r3_);
+          tmem_reg_tie(r0_);
+          tmem_reg_tie(r1_);
+          tmem_reg_tie(r2_);
 #pragma unroll
-        for (int c = 0; c < kBN; ++c)
-          if (kbase + c >= lim) s[c] = -CUDART_INF_F;
-      }
-      // The write before this one: (tile pt, step pj), or none.
-      int pt = -1, pj = 0;
-      if (t == 1 && j < nkt[0]) {
-        pt = 0;
-        pj = j;
-      } else if (j > 0) {
-        pt = (t == 0 && j - 1 < nkt[1]) ? 1 : t;
-        pj = j - 1;
-      }
-
-      constexpr int NPK = FP8V ? kBN / 4 : kBN / 2;   // P registers (and TMEM columns) per row
-      uint32_t pk[NPK];
-      bool done = false;
-      if (j > 0) {
-        // Common case: p = exp2(c s - m) against the running max m.  A row
-        // sum <= 2^8 bounds every p of the row by 2^8, i.e. its max grew by
-        // at most 8 and the exact path below would keep m: this P is its
-        // result.
-        const float sum = exp_pack<BF16, FP8V>(s, cs2, f2pack(-m, -m), pk);
-        // P complete before the wait for the buffer: the compiler may
-        // otherwise sink its conversions past the wait.
-#pragma unroll
-        for (int i = 0; i < NPK / 32; ++i) tmem_reg_tie(*reinterpret_cast<uint32_t(*)[32]>(&pk[32 * i]));
-        if (!__any_sync(0xffffffffu, !(sum <= kFastSumBound))) {
-          l += sum;
-          done = true;
-        }
-      }
-      if (pt >= 0) mbar_wait(&bar_pv[pt], pj & 1, p.err, 9);
-      tc_fence_after();
-      if (!done) {
-        // First tile, or a row of this warp may have grown by more than 2^8:
-        // tile max, O_t and l rescaled if the max grew by more than 2^8, p.
-        float mc[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mc[i] = fmaxf(s[2 * i], s[2 * i + 1]);
-#pragma unroll
-        for (int c = 16; c < kBN; c += 16) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) mc[i] = fmax3(mc[i], s[c + 2 * i], s[c + 2 * i + 1]);
-        }
-        const float mx = fmax3(fmax3(mc[0], mc[1], mc[2]), fmax3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
-        const float m_tile = mx * cs;
-        if (j == 0) {
-          m = m_tile;
-        } else {
-          const bool need = m_tile > m + kRescaleLog2;
-          const float m_new = need ? m_tile : m;
-          const float alpha = ex2_approx(m - m_new);
-          m = m_new;
-          l *= alpha;
-          const uint64_t a2 = f2pack(alpha, alpha);
-#pragma unroll
-          for (int c = 0; c < D / 16; ++c) {
-            uint32_t o[16];
-            tmem_ld16(tO + c * 16, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 16; e += 2) {
-              float lo, hi;
-              f2unpack(fmul2(f2pack(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2), lo, hi);
-              o[e] = __float_as_uint(lo);
-              o[e + 1] = __float_as_uint(hi);
-            }
-            tmem_st16(tO + c * 16, o);
+          for (int e = 0; e < 32; ++e) {
+            s[e] = __uint_as_float(r0_[e]);
+            s[32 + e] = __uint_as_float(r1_[e]);
+            s[64 + e] = __uint_as_float(r2_[e]);
+            s[96 + e] = __uint_as_float(r3_[e]);
           }
         }
-        const float mb = (m == -CUDART_INF_F) ? 0.f : m;
-        l += exp_pack<BF16, FP8V>(s, cs2, f2pack(-mb, -mb), pk);
-      }
-#pragma unroll
-      for (int i = 0; i < NPK / 16; ++i) tmem_st16(tP + i * 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[i * 16]));
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_pready);
-    }
+        // S_t,j is in registers: the tensor cores may overwrite it with S_t,j+1.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_sfree[t]);
 
-    if (p.n_splits > 1) {
+        const int kbase = (it.kt0 + j) * kBN;
+        if (kbase + kBN > p.Nk || (p.causal && kbase + kBN - 1 > r0)) {
+          const int lim = p.causal ? min(p.Nk, qrow + 1) : p.Nk;  // keys < lim are visible
+#pragma unroll
+          for (int c = 0; c < kBN; ++c)
+            if (kbase + c >= lim) s[c] = -CUDART_INF_F;
+        }
+        // The write before this one in this item (tile pt, that tile's PV
+        // number pn), or none: the item's first write, by tile 0, which
+        // instead waits for every PV of the items before (bar_item).  A
+        // parity wait must be at most one phase behind its barrier; tile 0
+        // waits on bar_item at every item and, with every item giving tile
+        // 0 keys and tile 1 at least as many (the launcher only walks
+        // several items per block then), no other wait of this loop can fall
+        // two phases behind either.
+        int pt = -1, pn = 0;
+        if (t == 1 && j < it.nkt[0]) {
+          pt = 0;
+          pn = pvb[0] + j;
+        } else if (j > 0) {
+          pt = (t == 0 && j - 1 < it.nkt[1]) ? 1 : t;
+          pn = pvb[pt] + j - 1;
+        }
+
+        constexpr int NPK = FP8V ? kBN / 4 : kBN / 2;   // P registers (and TMEM columns) per row
+        uint32_t pk[NPK];
+        bool done = false;
+        if (j > 0) {
+          // Common case: p = exp2(c s - m) against the running max m.  A row
+          // sum <= 2^8 bounds every p of the row by 2^8, i.e. its max grew by
+          // at most 8 and the exact path below would keep m: this P is its
+          // result.
+          const float sum = exp_pack<BF16, FP8V>(s, cs2, f2pack(-m, -m), pk);
+          // P complete before the wait for the buffer: the compiler may
+          // otherwise sink its conversions past the wait.
+#pragma unroll
+          for (int i = 0; i < NPK / 32; ++i) tmem_reg_tie(*reinterpret_cast<uint32_t(*)[32]>(&pk[32 * i]));
+          if (!__any_sync(0xffffffffu, !(sum <= kFastSumBound))) {
+            l += sum;
+            done = true;
+          }
+        }
+        if (pt >= 0)
+          mbar_wait(&bar_pv[pt], pn & 1, p.err, 9);
+        else if (ni > 0)
+          mbar_wait(bar_item, (ni - 1) & 1, p.err, 15);
+        tc_fence_after();
+        if (!done) {
+          // First tile, or a row of this warp may have grown by more than 2^8:
+          // tile max, O_t and l rescaled if the max grew by more than 2^8, p.
+          float mc[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mc[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+          for (int c = 16; c < kBN; c += 16) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mc[i] = fmax3(mc[i], s[c + 2 * i], s[c + 2 * i + 1]);
+          }
+          const float mx = fmax3(fmax3(mc[0], mc[1], mc[2]), fmax3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
+          const float m_tile = mx * cs;
+          if (j == 0) {
+            m = m_tile;
+          } else {
+            const bool need = m_tile > m + kRescaleLog2;
+            const float m_new = need ? m_tile : m;
+            const float alpha = ex2_approx(m - m_new);
+            m = m_new;
+            l *= alpha;
+            const uint64_t a2 = f2pack(alpha, alpha);
+#pragma unroll
+            for (int c = 0; c < D / 16; ++c) {
+              uint32_t o[16];
+              tmem_ld16(tO + c * 16, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 16; e += 2) {
+                float lo, hi;
+                f2unpack(fmul2(f2pack(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2), lo, hi);
+                o[e] = __float_as_uint(lo);
+                o[e + 1] = __float_as_uint(hi);
+              }
+              tmem_st16(tO + c * 16, o);
+            }
+          }
+          const float mb = (m == -CUDART_INF_F) ? 0.f : m;
+          l += exp_pack<BF16, FP8V>(s, cs2, f2pack(-mb, -mb), pk);
+        }
+#pragma unroll
+        for (int i = 0; i < NPK / 16; ++i) tmem_st16(tP + i * 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[i * 16]));
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_pready);
+      }
+
+      // Epilogue.  O_t is read before this warp's next P write, so the
+      // next item's first PV (which overwrites O_t) cannot start earlier.
       if (n > 0) {
-        mbar_wait(&bar_o[t], 0, p.err, 10);
+        mbar_wait(&bar_o[t], on & 1, p.err, 10);
+        ++on;
         tc_fence_after();
       }
-      store_partial<D>(p, tO, bh, split, qrow, m, l, n > 0);
-    } else if (n > 0) {
-      mbar_wait(&bar_o[t], 0, p.err, 10);
-      tc_fence_after();
-      store_o_lse<D, BF16>(p, tO, b, h, qrow, m, l);
+      if (p.n_splits > 1)
+        store_partial<D>(p, tO, it.bh, it.split, qrow, m, l, n > 0);
+      else if (n > 0)
+        store_o_lse<D, BF16>(p, tO, it.b, it.h, qrow, m, l);
+
+      ni += it.n_max > 0 ? 1 : 0;
+#pragma unroll
+      for (int u = 0; u < kNQT; ++u) pvb[u] += it.nkt[u];
     }
   }
 
@@ -1040,7 +1159,25 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
       return cudaErrorInvalidConfiguration;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CS::SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<static_cast<unsigned>(blocks), CS::THREADS, CS::SMEM, stream>>>(tq, tk, tv, p);
+    // Persistent blocks for all but about one round of the units (see
+    // sp_next), when every item gives tile 0 keys and tile 1 at least as
+    // many: no split, and no pair whose second tile lies wholly past Nq.
+    long long grid = blocks;
+    const int pair_rows = kNQT * kBM;
+    if (n_splits == 1 && (a.Nq % pair_rows == 0 || a.Nq % pair_rows > kBM)) {
+      int dev = 0, sms = 0;
+      e = cudaGetDevice(&dev);
+      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return e;
+      const long long units = static_cast<long long>((p.n_pairs + 1) / 2) * a.B * a.H;
+      const long long rounds = sms > 0 ? units / sms - 1 : 0;
+      if (rounds >= 1) {
+        p.grid_p = sms;
+        p.persist_units = static_cast<int>(rounds * sms);
+        grid = sms + 2 * (units - p.persist_units);
+      }
+    }
+    kern<<<static_cast<unsigned>(grid), CS::THREADS, CS::SMEM, stream>>>(tq, tk, tv, p);
   } else if constexpr (FP8V) {
     return cudaErrorInvalidValue;   // e5m2 V needs a P region of its own
   } else {
