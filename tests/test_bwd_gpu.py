@@ -76,6 +76,37 @@ def test_edge_cases(case):
     check(w, heads_limit=6, guard=512)
 
 
+# Enough heads that the backward kernels run blocks that walk work units
+# (the heaviest 128-row tile of a head with its lightest) plus one-tile
+# blocks for the rest: two or more rounds of units per SM on a 152-SM part.
+PERSIST = [
+    # dtype, layout, B, H, Nq, Nk, d, causal
+    ("bf16", "bhsd", 2, 160, 512, 512, 80, True),
+    ("fp16", "bhsd", 1, 200, 384, 384, 64, True),     # three tiles: the middle one alone in its unit
+    ("bf16", "bhsd", 1, 320, 700, 500, 80, False),    # ragged, Nq > Nk
+    ("bf16", "bhsd", 1, 256, 500, 900, 64, True),     # causal, Nq < Nk: key tiles past every query
+]
+
+
+@pytest.mark.parametrize("case", PERSIST, ids=["-".join(map(str, c)) for c in PERSIST])
+def test_persistent_units(case):
+    dt, layout, B, H, Nq, Nk, d, causal = case
+    w = W.custom(dt, layout, B, H, Nq, Nk, d, causal, std=0.5 if dt == "fp16" else 1.0, seed=Nq + H + 1,
+                 backward=True)
+    x = W.make_inputs(w, device="cuda", with_grad_output=True)
+    grads = run_fwd_bwd(w, x)
+    stats = {}
+    heads = [(b, h) for b in range(B) for h in range(H)]
+    for b, h in heads[:2] + heads[len(heads) // 2:len(heads) // 2 + 2] + heads[-2:]:
+        check_bwd_head(w, x, grads, b, h, stats)
+    for n in ("dq", "dk", "dv"):
+        assert torch.isfinite(grads[n]).all(), n
+    grads2 = run_fwd_bwd(w, x)
+    for n in ("dq", "dk", "dv"):
+        assert torch.equal(grads[n], grads2[n]), n
+    print(w.name, stats)
+
+
 def test_deterministic():
     w = W.custom("bf16", "bhsd", 2, 3, 700, 900, 80, True, seed=3, backward=True)
     x = W.make_inputs(w, device="cuda")
