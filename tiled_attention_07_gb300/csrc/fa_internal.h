@@ -86,7 +86,7 @@ __host__ __device__ inline void chunked_order(int lin, int n_tiles, int BH, int*
 }
 
 // Encodes a 4-D TMA map {d, rows, H, B} with a {chunk_cols(d), 128, 1, 1}
-// box and the matching swizzle.  Returns false if cuTensorMapEncodeTiled rejects it.
+// box and the matching swizzle.  Returns false if the driver rejects it.
 bool make_tile_map(CUtensorMap* map, const Tensor4& t, int d, int rows, int H, int B, bool bf16);
 // Tensor map of a transposed e5m2 V: boxes of 128 keys (one 128-byte row,
 // 128-byte swizzle) by d rows.
