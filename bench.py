@@ -166,13 +166,19 @@ KERNEL_SOURCES = {
 
 
 def kernel_source_hash(kernel: str) -> str:
-    """Short SHA-256 of the CUDA sources `kernel` is built from."""
+    """Short SHA-256 of the code of the CUDA sources `kernel` is built from:
+    // comments and blank lines are left out, so that editing a comment does
+    not make a traffic capture stale (the sources hold no block comments and
+    no string containing //)."""
     import hashlib
 
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "tiled_attention_07_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "tiled_attention_07_gb300", "csrc", name), encoding="utf-8") as f:
+            for line in f:
+                code = line.split("//", 1)[0].rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

@@ -9,6 +9,11 @@
 // sm_scale * 1.44269504, p = exp2(qk - m), alpha = exp2(m_old - m_new)), and the
 // delayed normalisation of FA-2 (O divided by the final l only).
 //
+// Two kernels.  fwd_sp_kernel (d <= 96, further below) gives P TMEM columns
+// of its own, splits the issuers by MMA kind (one warp every S, one every PV),
+// lets blocks walk several work units, and has an e5m2-V variant; fwd_kernel
+// (d = 128, next) is described here.
+//
 // GB300 design (one CTA = two 128-row query tiles of one (b, h)):
 //   warps 0-3  softmax / correction / epilogue of query tile 0 (one row each)
 //   warps 4-7  the same for query tile 1
