@@ -170,11 +170,17 @@ def kernel_source_hash(kernel: str) -> str:
     // comments and blank lines are left out, so that editing a comment does
     not make a traffic capture stale (the sources hold no block comments and
     no string containing //)."""
+    return code_digest(os.path.join(ROOT, "tiled_attention_07_gb300", "csrc", name) for name in KERNEL_SOURCES[kernel])
+
+
+def code_digest(paths) -> str:
+    """Short SHA-256 of the given files' lines with // comments and blank
+    lines left out."""
     import hashlib
 
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "tiled_attention_07_gb300", "csrc", name), encoding="utf-8") as f:
+    for path in paths:
+        with open(path, encoding="utf-8") as f:
             for line in f:
                 code = line.split("//", 1)[0].rstrip()
                 if code:

@@ -1,0 +1,44 @@
+"""bench.py's own contract, on CPU: the reference arm's JSON line, the
+traffic table lookup and the code digest that ties it to the sources."""
+
+import json
+import os
+import subprocess
+import sys
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_reference_arm_prints_one_json_line():
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+           "bf16_b4_h12_n512_d64_causal", "--steps", "2", "--warmup", "3"]
+    out = subprocess.run(cmd, capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    lines = [l for l in out.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "TFLOP/s" and d["value"] > 0
+    assert d["steps"] == 2 and d["warmup"] >= 3 and d["higher_is_better"] is True
+    assert d["metric"] == bench.METRIC and d["dtype"] == "f64"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_code_digest_ignores_comments_only(tmp_path):
+    a = tmp_path / "a.cu"
+    a.write_text("int f() {\n  return 1;  // one\n}\n")
+    d0 = bench.code_digest([a])
+    a.write_text("// a new comment\nint f() {\n\n  return 1;  // still one\n}\n")
+    assert bench.code_digest([a]) == d0
+    a.write_text("int f() {\n  return 2;\n}\n")
+    assert bench.code_digest([a]) != d0
+
+
+def test_committed_traffic_follows_the_sources(monkeypatch):
+    for k in ("fwd", "bwd_dkdv", "bwd_dq"):
+        assert bench.committed_traffic(k) > 0, k   # the table matches the committed sources
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda kernel: "0000000000000000")
+    assert bench.committed_traffic("bwd_dkdv") is None
