@@ -49,7 +49,13 @@ def check(w, heads_limit=10 ** 9, guard=0):
 
 
 def test_bench_workload_backward_sampled_heads():
-    stats = check(W.WORKLOADS[W.BENCH_WORKLOAD], heads_limit=2)
+    # 8 seeded heads including (0, 0) and (B-1, H-1)
+    stats = check(W.WORKLOADS[W.BENCH_WORKLOAD], heads_limit=8)
+    print(stats)
+
+
+def test_long_causal_d64_backward_sampled_heads():
+    stats = check(W.WORKLOADS["bf16_b4_h20_n4096_d64_causal"], heads_limit=8)
     print(stats)
 
 
