@@ -168,10 +168,10 @@ FA_API fa_status fa_fwd_split(const void* q, const void* k, const void* v, void*
  * float32 accumulation.  LSE is exact, as in fa_fwd; O differs from the
  * exact result by at most about 2^-3 * max |v| over the row's keys (the
  * rounding of P, relative 2^-3) plus the 16-bit rounding of O.
- * d in {64, 80}; d = 128 gives FA_ERR_UNSUPPORTED (with d = 128 the tensor
- * memory has no room for P next to S and O of two query tiles).  Errors as
- * fa_fwd; vt_ld out of range gives FA_ERR_INVALID_ARG.  One launch on
- * `stream`.
+ * d in {64, 80, 128} (at d = 128 the 8-bit P is written over the first 32
+ * columns of its tile's S in tensor memory, as the 16-bit P is there).
+ * Errors as fa_fwd; vt_ld out of range gives FA_ERR_INVALID_ARG.  One launch
+ * on `stream`.
  */
 FA_API fa_status fa_fwd_fp8v(const void* q, const void* k, const void* vt, void* o, float* lse,
                       int B, int H, int Nq, int Nk, int d, int64_t vt_ld, float sm_scale,

@@ -88,7 +88,6 @@ def fwd8(L, q=FAKE, k=FAKE, vt=FAKE, o=FAKE, lse=FAKE, B=1, H=1, Nq=128, Nk=128,
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(d=128), fa.FA_ERR_UNSUPPORTED),       # no room for P next to S and O
     (dict(d=96), fa.FA_ERR_UNSUPPORTED),
     (dict(dtype=fa.FA_FP32), fa.FA_ERR_UNSUPPORTED),
     (dict(Nk=100, ld=100), fa.FA_ERR_INVALID_ARG),   # row stride not a multiple of 16 bytes

@@ -124,6 +124,8 @@ def check_loose(w, pad_code=0):
     ("fp16", 1, 2, 700, 700, 80, True),
     ("fp16", 2, 1, 300, 300, 80, False),     # ragged key tail, ld = 304
     ("bf16", 1, 3, 640, 640, 64, True),
+    ("fp16", 1, 2, 513, 700, 128, False),    # d = 128: P over the S columns
+    ("fp16", 2, 1, 600, 600, 128, True),
 ])
 def test_tight_against_e5m2_oracle(dtype, B, H, Nq, Nk, d, causal):
     w = W.custom(dtype, "bhsd", B, H, Nq, Nk, d, causal, seed=Nq + Nk + d)
@@ -135,6 +137,7 @@ def test_tight_against_e5m2_oracle(dtype, B, H, Nq, Nk, d, causal):
     ("fp16", 1, 2, 1000, 2500, 80, False),   # the cross-attention shape, ragged keys
     ("bf16", 2, 2, 129, 77, 64, True),       # one ragged key tile
     ("fp16", 1, 1, 1, 1000, 64, False),      # a single query row
+    ("bf16", 1, 2, 1000, 1000, 128, True),
 ])
 def test_loose_against_exact(dtype, B, H, Nq, Nk, d, causal):
     w = W.custom(dtype, "bhsd", B, H, Nq, Nk, d, causal, seed=3 * Nq + Nk)
@@ -148,13 +151,3 @@ def test_padding_bytes_are_not_read():
     o, lse = run(w, x)
     assert torch.isfinite(o).all() and torch.isfinite(lse).all()
     print(check_loose(w, pad_code=0x7F))
-
-
-def test_d128_is_unsupported():
-    w = W.custom("bf16", "bhsd", 1, 1, 128, 128, 128, False, seed=1)
-    x = W.fp8v_inputs(w, "cuda")
-    o = torch.empty_like(x["q"])
-    lse = torch.empty(fa.lse_shape(x["q"]), dtype=torch.float32, device="cuda")
-    with pytest.raises(fa.FaError) as e:
-        fa.fa_fwd_fp8v(x["q"], x["k"], x["vt"], o, lse, w.sm_scale, w.causal)
-    assert e.value.code == fa.FA_ERR_UNSUPPORTED

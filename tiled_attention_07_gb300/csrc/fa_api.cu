@@ -152,7 +152,6 @@ fa_status fwd_fp8v_impl(const void* q, const void* k, const void* vt, void* o, f
                         int Nk, int d, int64_t ld, float sm_scale, int causal, fa_dtype dtype, void* stream) {
   fa_status st = check_common(B, H, Nq, Nk, d, sm_scale, causal, dtype);
   if (st != FA_OK) return st;
-  if (d == 128) return FA_ERR_UNSUPPORTED;   // no TMEM columns for a separate P (see include/fa.h)
   if (ld < Nk || ld % 16 != 0 || ld >= (int64_t(1) << 32)) return FA_ERR_INVALID_ARG;
   if (B == 0 || H == 0 || Nq == 0) return FA_OK;
   const Tensor4 tq = contiguous(q, H, Nq, d), tk = contiguous(k, H, Nk, d), to = contiguous(o, H, Nq, d);

@@ -242,7 +242,7 @@ __device__ __forceinline__ float exp_pack(const float (&s)[kBN], uint64_t cs2, u
   return a0 + a1;
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool FP8V>
 __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -337,11 +337,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           nfill = f;
           break;
         }
-        mbar_arrive_expect_tx(&bar_full[s], C::TILE);
         const int j = kt0 + (f >> 1);
-        const CUtensorMap* map = (f & 1) ? &tmV : &tmK;
-        for (int c = 0; c < C::G::NCH; ++c)
-          tma_load_4d(sKV + s * C::TILE + c * C::G::CHB, map, &bar_full[s], c * C::G::CC, j * kBN, h, b);
+        if (FP8V && (f & 1)) {
+          // V_j^T: D rows of 128 keys, one box
+          mbar_arrive_expect_tx(&bar_full[s], D * kBN);
+          tma_load_4d(sKV + s * C::TILE, &tmV, &bar_full[s], j * kBN, 0, h, b);
+        } else {
+          mbar_arrive_expect_tx(&bar_full[s], C::TILE);
+          const CUtensorMap* map = (f & 1) ? &tmV : &tmK;
+          for (int c = 0; c < C::G::NCH; ++c)
+            tma_load_4d(sKV + s * C::TILE + c * C::G::CHB, map, &bar_full[s], c * C::G::CC, j * kBN, h, b);
+        }
       }
       // Drain: the last fill of every slot has landed before the CTA exits.
       for (int f = max(0, nfill - C::NSTAGE); f < nfill; ++f)
@@ -394,7 +400,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         mbar_wait(&bar_turn[t], (t == 0 ? j : j + 1) & 1, p.err, 12);
         __syncwarp();
         tc_fence_after();
-        if (pv) issue_pv<D, BF16>(tmem + 256 + t * 128, tmem + t * 128, skv_addr + (fv % C::NSTAGE) * C::TILE, j > 0);
+        if (pv) {
+          if constexpr (FP8V)
+            issue_pv_f8<D>(tmem + 256 + t * 128, tmem + t * 128, skv_addr + (fv % C::NSTAGE) * C::TILE, j > 0);
+          else
+            issue_pv<D, BF16>(tmem + 256 + t * 128, tmem + t * 128, skv_addr + (fv % C::NSTAGE) * C::TILE, j > 0);
+        }
         if (sn) issue_s<D, BF16>(tmem + t * 128, sq_addr + t * C::TILE, skv_addr + (fk % C::NSTAGE) * C::TILE);
         if (elect_one()) {
           mbar_arrive(&bar_turn[1 - t]);
@@ -421,6 +432,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     const uint32_t tS = tmem + lane_off + t * 128;
     const uint32_t tO = tmem + lane_off + 256 + t * 128;
     const float cs = p.scale_log2;
+    // scores per 16-column P store: 32 as 16-bit pairs, 64 as e5m2 quads
+    constexpr int kPChunk = FP8V ? 64 : 32;
 
     float m = -CUDART_INF_F;  // running max of the scaled scores (log2 domain)
     float l = 0.f;            // running sum of exp2(score - m)
@@ -463,18 +476,28 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 8; ++i) mc[i] = -CUDART_INF_F;
 #pragma unroll
-        for (int i = 0; i < kBN / 32; ++i) {
+        for (int i = 0; i < kBN / kPChunk; ++i) {
           uint32_t pk[16];
+          float q0 = 0.f, q1 = 0.f;   // e5m2: the previous pair, waiting for its partner
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int c = i * 32 + 2 * e;
+          for (int e = 0; e < kPChunk / 2; ++e) {
+            const int c = i * kPChunk + 2 * e;
             mc[e & 7] = fmax3(mc[e & 7], s[c], s[c + 1]);
             float x0, x1;
             f2unpack(ffma2(f2pack(s[c], s[c + 1]), cs2, nm2), x0, x1);
             const float p0 = ex2_approx(x0);
             const float p1 = ex2_approx(x1);
             acc[e & 3] = fadd2(acc[e & 3], f2pack(p0, p1));
-            pk[e] = pack2<BF16>(p0, p1);
+            if constexpr (FP8V) {
+              if (e & 1) {
+                pk[e >> 1] = pack4_e5m2(q0, q1, p0, p1);
+              } else {
+                q0 = p0;
+                q1 = p1;
+              }
+            } else {
+              pk[e] = pack2<BF16>(p0, p1);
+            }
           }
           tmem_st16(tS + i * 16, pk);
         }
@@ -532,17 +555,27 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         const uint64_t nm2 = f2pack(-mb, -mb);
         uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-        for (int i = 0; i < kBN / 32; ++i) {
+        for (int i = 0; i < kBN / kPChunk; ++i) {
           uint32_t pk[16];
+          float q0 = 0.f, q1 = 0.f;
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int c = i * 32 + 2 * e;
+          for (int e = 0; e < kPChunk / 2; ++e) {
+            const int c = i * kPChunk + 2 * e;
             float x0, x1;
             f2unpack(ffma2(f2pack(s[c], s[c + 1]), cs2, nm2), x0, x1);
             const float p0 = ex2_approx(x0);
             const float p1 = ex2_approx(x1);
             acc[e & 3] = fadd2(acc[e & 3], f2pack(p0, p1));
-            pk[e] = pack2<BF16>(p0, p1);
+            if constexpr (FP8V) {
+              if (e & 1) {
+                pk[e >> 1] = pack4_e5m2(q0, q1, p0, p1);
+              } else {
+                q0 = p0;
+                q1 = p1;
+              }
+            } else {
+              pk[e] = pack2<BF16>(p0, p1);
+            }
           }
           tmem_st16(tS + i * 16, pk);
         }
@@ -1183,10 +1216,8 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
       }
     }
     kern<<<static_cast<unsigned>(grid), CS::THREADS, CS::SMEM, stream>>>(tq, tk, tv, p);
-  } else if constexpr (FP8V) {
-    return cudaErrorInvalidValue;   // e5m2 V needs a P region of its own
   } else {
-    auto kern = fwd_kernel<D, BF16>;
+    auto kern = fwd_kernel<D, BF16, FP8V>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     kern<<<static_cast<unsigned>(blocks), C::THREADS, C::SMEM, stream>>>(tq, tk, tv, p);
@@ -1219,6 +1250,8 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
     switch (a.d) {
       case 64: return a.bf16 ? launch_fwd_t<64, true, true>(a, stream) : launch_fwd_t<64, false, true>(a, stream);
       case 80: return a.bf16 ? launch_fwd_t<80, true, true>(a, stream) : launch_fwd_t<80, false, true>(a, stream);
+      case 128:
+        return a.bf16 ? launch_fwd_t<128, true, true>(a, stream) : launch_fwd_t<128, false, true>(a, stream);
       default: return cudaErrorInvalidValue;
     }
   }
