@@ -126,6 +126,7 @@ def check_loose(w, pad_code=0):
     ("bf16", 1, 3, 640, 640, 64, True),
     ("fp16", 1, 2, 513, 700, 128, False),    # d = 128: P over the S columns
     ("fp16", 2, 1, 600, 600, 128, True),
+    ("fp16", 1, 320, 512, 512, 80, True),    # enough heads for the work-unit blocks
 ])
 def test_tight_against_e5m2_oracle(dtype, B, H, Nq, Nk, d, causal):
     w = W.custom(dtype, "bhsd", B, H, Nq, Nk, d, causal, seed=Nq + Nk + d)
@@ -138,6 +139,7 @@ def test_tight_against_e5m2_oracle(dtype, B, H, Nq, Nk, d, causal):
     ("bf16", 2, 2, 129, 77, 64, True),       # one ragged key tile
     ("fp16", 1, 1, 1, 1000, 64, False),      # a single query row
     ("bf16", 1, 2, 1000, 1000, 128, True),
+    ("bf16", 2, 160, 768, 768, 64, True),    # work-unit blocks, an odd middle pair
 ])
 def test_loose_against_exact(dtype, B, H, Nq, Nk, d, causal):
     w = W.custom(dtype, "bhsd", B, H, Nq, Nk, d, causal, seed=3 * Nq + Nk)
