@@ -36,9 +36,10 @@
  * - Causal masking is top-left aligned: key j is visible to query i iff
  *   j <= i, also when Nq != Nk.
  * - Requirements (checked before any launch): B, H, Nq >= 0; Nk >= 1;
- *   d in {64, 80, 128}; pointers non-null and 16-byte aligned; strides
- *   (in bytes) multiples of 16; sm_scale finite and > 0.  B*H == 0 or Nq == 0 is a
- *   no-op returning FA_OK.  Other d give FA_ERR_UNSUPPORTED.
+ *   Nq, Nk <= FA_MAX_SEQLEN; B*H < 2^31; d in {64, 80, 128}; pointers
+ *   non-null and 16-byte aligned; strides positive, in bytes multiples of 16
+ *   and below 2^40 (the TMA limit); sm_scale finite and > 0.  B*H == 0 or
+ *   Nq == 0 is a no-op returning FA_OK.  Other d give FA_ERR_UNSUPPORTED.
  * - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *   default stream) and never synchronise.  The return value reports
  *   argument errors (nothing launched) and launch errors (FA_ERR_CUDA).
@@ -75,6 +76,11 @@ typedef enum {
 /* Element types.  The attention entry points take FA_FP16 and FA_BF16 (other
  * values give FA_ERR_UNSUPPORTED); fa_softmax_rows also takes FA_FP32. */
 typedef enum { FA_FP16 = 0, FA_BF16 = 1, FA_FP32 = 2 } fa_dtype;
+
+/* Longest Nq or Nk the attention entry points take (2^30).  A longer
+ * sequence does not fit the device's memory at any supported head dim, and
+ * the bound keeps every row index and tile count in int arithmetic. */
+#define FA_MAX_SEQLEN (1 << 30)
 
 /* Element strides of one [B, H, seq, d] tensor; the d stride is always 1. */
 typedef struct {

@@ -21,11 +21,21 @@ def header_symbols():
 
 
 @pytest.fixture(scope="module")
-def L():
+def lib():
     if not os.path.exists(fa.LIB_PATH):
         from tiled_attention_07_gb300 import build
         build.build()
     return fa.lib()
+
+
+@pytest.fixture(scope="module")
+def L(lib):
+    # The argument checks below pass fake device addresses.  Should a check
+    # ever let one through, a launch would follow, so these run only where no
+    # GPU is visible.
+    if torch.cuda.is_available():
+        pytest.skip("fake device addresses: argument checks run on a machine without a GPU")
+    return lib
 
 
 def test_header_declares_the_binding_symbols():
@@ -33,19 +43,19 @@ def test_header_declares_the_binding_symbols():
     assert sorted(syms) == sorted(fa.EXPORTED_SYMBOLS)
 
 
-def test_library_exports_every_declared_symbol(L):
+def test_library_exports_every_declared_symbol(lib):
     for s in header_symbols():
-        assert hasattr(L, s), f"libfa.so does not export {s}"
+        assert hasattr(lib, s), f"libfa.so does not export {s}"
 
 
-def test_status_strings_and_version(L):
+def test_status_strings_and_version(lib):
     assert fa.fa_version() == "0.1.0"
     for code in range(6):
         assert fa.fa_status_string(code).startswith("FA_")
     assert "unknown" in fa.fa_status_string(99)
 
 
-def test_workspace_bytes(L):
+def test_workspace_bytes(lib):
     assert fa.fa_bwd_workspace_bytes(4, 32, 8192, 8192, 80) == 2 * 4 * 4 * 32 * 8192
     assert fa.fa_bwd_workspace_bytes(1, 16, 1000, 2500, 80) == 2 * 4 * 16 * 1024
     assert fa.fa_bwd_workspace_bytes(0, 16, 1000, 2500, 80) == 0
@@ -159,7 +169,7 @@ def test_binding_refuses_cpu_tensors():
         fa.attention_forward(q, q, q, 0.125, False)
 
 
-def test_split_workspace_bytes(L):
+def test_split_workspace_bytes(lib):
     # float32 O_s (d columns) and lse_s per split, rows padded to 128-row tiles
     assert fa.fa_fwd_split_workspace_bytes(1, 16, 1000, 80, 4) == 4 * 4 * 16 * 1024 * 81
     assert fa.fa_fwd_split_workspace_bytes(4, 12, 512, 64, 2) == 4 * 2 * 48 * 512 * 65
@@ -219,3 +229,63 @@ def test_softmax_rows_rejects_bad_arguments(L):
     assert sm(z=FAKE + 16, T=96) == fa.FA_ERR_INVALID_ARG   # overlapping, not identical
     assert sm(z=FAKE, xs=100, zs=104) == fa.FA_ERR_INVALID_ARG   # same base, other stride
     assert sm(rows=0) == fa.FA_OK
+
+
+# Sizes whose strides or workspace sizes overflow 64-bit arithmetic are
+# rejected, never wrapped into something that passes a check.
+I32_MAX = 2 ** 31 - 1
+SIZE_MAX = 2 ** 64 - 1
+
+
+def test_sequence_length_limit(L):
+    limit = 1 << 30
+    assert fwd(L, Nq=limit + 1) == fa.FA_ERR_INVALID_ARG
+    assert fwd(L, Nk=limit + 1) == fa.FA_ERR_INVALID_ARG
+    assert fwd(L, Nq=I32_MAX, Nk=I32_MAX) == fa.FA_ERR_INVALID_ARG
+    assert fwd8(L, Nq=limit + 1) == fa.FA_ERR_INVALID_ARG
+    assert split(L, Nk=limit + 1) == fa.FA_ERR_INVALID_ARG
+    ptrs = [FAKE] * 9
+    assert L.fa_bwd(*ptrs, 1, 1, limit + 1, 128, 64, 0.125, 0, fa.FA_BF16, FAKE, SIZE_MAX, None) == \
+        fa.FA_ERR_INVALID_ARG
+
+
+def test_contiguous_strides_that_overflow_are_rejected(L):
+    # H * Nq * d = 2^30 * 2^30 * 64 elements: no int64 wrap, a stride past 2^40 bytes
+    assert fwd(L, B=1, H=1 << 30, Nq=1 << 30, Nk=128) == fa.FA_ERR_INVALID_ARG
+    # the batch stride H * Nq * d reaches 2^39 elements (2^40 bytes)
+    assert fwd(L, B=2, H=(1 << 39) // (1024 * 64), Nq=1024, Nk=128) == fa.FA_ERR_INVALID_ARG
+
+
+def test_strided_stride_limit(L):
+    lay = fa.Layout()
+    for n in ("q", "k", "v", "o"):
+        setattr(lay, n, fa.Strides(128 * 64, 128 * 64, 64))
+    args = [FAKE] * 5 + [2, 1, 128, 128, 64, 0.125, 0, fa.FA_BF16]
+    lay.q = fa.Strides(1 << 39, 128 * 64, 64)            # 2^40 bytes: past the TMA limit
+    assert L.fa_fwd_strided(*args, ctypes.byref(lay), None) == fa.FA_ERR_INVALID_ARG
+    lay.q = fa.Strides(2 ** 63 - 8, 128 * 64, 64)        # doubled, wraps negative
+    assert L.fa_fwd_strided(*args, ctypes.byref(lay), None) == fa.FA_ERR_INVALID_ARG
+    lay.q = fa.Strides(-(1 << 20), 128 * 64, 64)
+    assert L.fa_fwd_strided(*args, ctypes.byref(lay), None) == fa.FA_ERR_INVALID_ARG
+
+
+def test_fp8v_batch_stride_limit(L):
+    # V^T batch stride = ld * d * H bytes must stay below 2^40
+    ld = 1 << 24
+    assert fwd8(L, B=2, H=(1 << 40) // (ld * 64), Nk=128, ld=ld) == fa.FA_ERR_INVALID_ARG
+    assert fwd8(L, B=2, H=I32_MAX // 2, Nk=128, ld=(1 << 32) - 16, d=128) == fa.FA_ERR_INVALID_ARG
+
+
+def test_workspace_sizes_saturate(lib):
+    assert fa.fa_bwd_workspace_bytes(I32_MAX, I32_MAX, I32_MAX, 1, 64) == SIZE_MAX
+    assert fa.fa_fwd_split_workspace_bytes(I32_MAX, I32_MAX, 1 << 30, 128, 64) == SIZE_MAX
+    # no saturation at ordinary sizes
+    assert fa.fa_bwd_workspace_bytes(4, 32, 8192, 8192, 80) == 2 * 4 * 4 * 32 * 8192
+
+
+def test_softmax_span_overflow_is_rejected(L):
+    # (rows - 1) * stride * 4 bytes overflows int64
+    assert L.fa_softmax_rows(FAKE, FAKE + (1 << 24), None, 1 << 20, 128, 2 ** 45, 2 ** 45, fa.FA_FP32,
+                             None) == fa.FA_ERR_INVALID_ARG
+    assert L.fa_softmax_rows(FAKE, FAKE + (1 << 24), None, 2, 128, 2 ** 62, 128, fa.FA_FP32,
+                             None) == fa.FA_ERR_INVALID_ARG

@@ -9,6 +9,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <limits>
 #include <mutex>
 
 namespace fa {
@@ -66,20 +67,36 @@ int* err_word(cudaError_t* e) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// a * b for a, b >= 0; -1 (an invalid stride) when either is negative or the
+// product does not fit in int64.
+int64_t mul_nonneg(int64_t a, int64_t b) {
+  if (a < 0 || b < 0) return -1;
+  if (a != 0 && b > std::numeric_limits<int64_t>::max() / a) return -1;
+  return a * b;
+}
+
+// a * b saturated at SIZE_MAX, a size no buffer has.
+size_t mul_sat(size_t a, size_t b) {
+  return a != 0 && b > std::numeric_limits<size_t>::max() / a ? std::numeric_limits<size_t>::max() : a * b;
+}
+
+// TMA takes strides below 2^40 bytes.
+constexpr int64_t kMaxStrideBytes = int64_t(1) << 40;
+
 // A [B, H, rows, d] tensor view is valid for TMA and 16-byte vector access.
 bool valid_tensor(const Tensor4& t) {
   if (t.ptr == nullptr || !aligned16(t.ptr)) return false;
   const int64_t st[3] = {t.sb, t.sh, t.ss};
   for (int64_t s : st) {
-    if (s <= 0) return false;
+    if (s <= 0 || s >= kMaxStrideBytes / 2) return false;
     if ((s * 2) % 16 != 0) return false;
-    if (s * 2 >= (int64_t(1) << 40)) return false;
   }
   return true;
 }
 
 fa_status check_common(int B, int H, int Nq, int Nk, int d, float sm_scale, int causal, fa_dtype dtype) {
   if (B < 0 || H < 0 || Nq < 0 || Nk < 1) return FA_ERR_INVALID_ARG;
+  if (Nq > FA_MAX_SEQLEN || Nk > FA_MAX_SEQLEN) return FA_ERR_INVALID_ARG;
   if (!(std::isfinite(sm_scale)) || !(sm_scale > 0.f)) return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if (dtype != FA_FP16 && dtype != FA_BF16) return FA_ERR_UNSUPPORTED;
@@ -88,12 +105,14 @@ fa_status check_common(int B, int H, int Nq, int Nk, int d, float sm_scale, int 
   return FA_OK;
 }
 
+// Strides of a contiguous [B, H, n, d] tensor; one that overflows comes out
+// negative, which valid_tensor rejects.
 Tensor4 contiguous(const void* p, int H, int n, int d) {
   Tensor4 t;
   t.ptr = p;
   t.ss = d;
-  t.sh = static_cast<int64_t>(n) * d;
-  t.sb = static_cast<int64_t>(H) * n * d;
+  t.sh = mul_nonneg(n, d);
+  t.sb = mul_nonneg(mul_nonneg(H, n), d);
   return t;
 }
 
@@ -108,7 +127,10 @@ Tensor4 strided(const void* p, const fa_strides& s) {
 
 size_t split_ws_bytes(int B, int H, int Nq, int d, int n_splits) {
   if (n_splits < 2 || B <= 0 || H <= 0 || Nq <= 0 || d <= 0) return 0;
-  return sizeof(float) * static_cast<size_t>(n_splits) * B * H * nq_pad(Nq) * (d + 1);
+  size_t n = sizeof(float) * static_cast<size_t>(n_splits);
+  n = mul_sat(n, static_cast<size_t>(B) * static_cast<size_t>(H));
+  n = mul_sat(n, static_cast<size_t>(nq_pad(Nq)));
+  return mul_sat(n, static_cast<size_t>(d) + 1);
 }
 
 fa_status fwd_impl(const Tensor4& q, const Tensor4& k, const Tensor4& v, const Tensor4& o, float* lse, int B, int H,
@@ -157,6 +179,8 @@ fa_status fwd_fp8v_impl(const void* q, const void* k, const void* vt, void* o, f
   const Tensor4 tq = contiguous(q, H, Nq, d), tk = contiguous(k, H, Nk, d), to = contiguous(o, H, Nq, d);
   if (!valid_tensor(tq) || !valid_tensor(tk) || !valid_tensor(to)) return FA_ERR_INVALID_ARG;
   if (vt == nullptr || !aligned16(vt)) return FA_ERR_INVALID_ARG;
+  const int64_t vt_sb = mul_nonneg(ld * d, H);   // ld < 2^32 and d <= 128: ld * d fits
+  if (vt_sb < 0 || vt_sb >= kMaxStrideBytes) return FA_ERR_INVALID_ARG;
   if (lse == nullptr || !aligned16(lse)) return FA_ERR_INVALID_ARG;
   if (get_encode() == nullptr) return FA_ERR_CUDA;
   cudaError_t e;
@@ -168,7 +192,7 @@ fa_status fwd_fp8v_impl(const void* q, const void* k, const void* vt, void* o, f
   a.v.ptr = vt;
   a.v.ss = ld;
   a.v.sh = ld * d;
-  a.v.sb = ld * d * H;
+  a.v.sb = vt_sb;
   a.o = to;
   a.lse = lse;
   a.B = B;
@@ -188,7 +212,8 @@ fa_status fwd_fp8v_impl(const void* q, const void* k, const void* vt, void* o, f
 
 size_t ws_bytes(int B, int H, int Nq) {
   if (B <= 0 || H <= 0 || Nq <= 0) return 0;
-  return 2 * sizeof(float) * static_cast<size_t>(B) * H * nq_pad(Nq);
+  const size_t rows = mul_sat(static_cast<size_t>(B) * static_cast<size_t>(H), static_cast<size_t>(nq_pad(Nq)));
+  return mul_sat(2 * sizeof(float), rows);
 }
 
 fa_status bwd_impl(const Tensor4& q, const Tensor4& k, const Tensor4& v, const Tensor4& o, const Tensor4& dout,

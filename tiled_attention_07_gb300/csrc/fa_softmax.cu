@@ -24,6 +24,7 @@
 #include <math_constants.h>
 
 #include <algorithm>
+#include <limits>
 
 namespace fa {
 namespace {
@@ -330,15 +331,18 @@ extern "C" fa_status fa_softmax_rows(const void* x, void* z, float* lse, int row
   if (!aligned(x) || !aligned(z)) return FA_ERR_INVALID_ARG;
   if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_INVALID_ARG;
   if (x_row_stride < T || z_row_stride < T) return FA_ERR_INVALID_ARG;
+  // Each tensor's byte span, (rows - 1) * stride + T elements, must fit in int64.
+  const int64_t max_stride = (std::numeric_limits<int64_t>::max() / esz - T) / std::max(rows - 1, 1);
+  if (x_row_stride > max_stride || z_row_stride > max_stride) return FA_ERR_INVALID_ARG;
   if ((x_row_stride * esz) % 16 != 0 || (z_row_stride * esz) % 16 != 0) return FA_ERR_INVALID_ARG;
   if (static_cast<int64_t>(rows) * kMaxCluster > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
   // z may only alias x exactly (in place): every element is read before the
   // same thread writes it, and no thread reads another's elements.
-  const uint8_t* xb = static_cast<const uint8_t*>(x);
-  const uint8_t* zb = static_cast<const uint8_t*>(z);
+  const uintptr_t xb = reinterpret_cast<uintptr_t>(x);
+  const uintptr_t zb = reinterpret_cast<uintptr_t>(z);
   const int64_t xspan = ((static_cast<int64_t>(rows) - 1) * x_row_stride + T) * esz;
   const int64_t zspan = ((static_cast<int64_t>(rows) - 1) * z_row_stride + T) * esz;
-  const bool overlap = xb < zb + zspan && zb < xb + xspan;
+  const bool overlap = xb < zb + static_cast<uintptr_t>(zspan) && zb < xb + static_cast<uintptr_t>(xspan);
   if (overlap && !(xb == zb && x_row_stride == z_row_stride)) return FA_ERR_INVALID_ARG;
 
   SoftmaxParams p;
