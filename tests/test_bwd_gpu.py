@@ -129,9 +129,16 @@ def test_no_queries_gives_zero_dk_dv():
     dq = torch.empty_like(q)
     dk = torch.full_like(k, float("nan"))
     dv = torch.full_like(k, float("nan"))
-    # Nq = 0: lse and the query-side tensors are never read
-    fa.fa_bwd(q, k, k, q, q, torch.zeros(1, 2, 1, device="cuda"), dq, dk, dv, 0.125, False,
-              torch.empty(16, dtype=torch.uint8, device="cuda"))
+    fa.fa_bwd(q, k, k, q, q, lse, dq, dk, dv, 0.125, False, torch.empty(16, dtype=torch.uint8, device="cuda"))
+    torch.cuda.synchronize()
+    assert torch.all(dk == 0) and torch.all(dv == 0)
+    # Through the C ABI, Nq = 0 reads neither lse nor the workspace: both may be null.
+    dk.fill_(float("nan"))
+    dv.fill_(float("nan"))
+    rc = fa.lib().fa_bwd(q.data_ptr(), k.data_ptr(), k.data_ptr(), q.data_ptr(), q.data_ptr(), None, dq.data_ptr(),
+                         dk.data_ptr(), dv.data_ptr(), 1, 2, 0, 200, 64, 0.125, 0, fa.FA_BF16, None, 0,
+                         torch.cuda.current_stream().cuda_stream)
+    assert rc == fa.FA_OK
     torch.cuda.synchronize()
     assert torch.all(dk == 0) and torch.all(dv == 0)
 

@@ -179,9 +179,9 @@ def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
-def _stream(stream) -> Optional[int]:
+def _stream(stream, device=None) -> Optional[int]:
     if stream is None:
-        return torch.cuda.current_stream().cuda_stream
+        return torch.cuda.current_stream(device).cuda_stream
     if isinstance(stream, torch.cuda.Stream):
         return stream.cuda_stream
     return int(stream)
@@ -193,24 +193,61 @@ def _check_cuda(*ts):
             raise ValueError("fa_* entry points take CUDA tensors only (no CPU path)")
 
 
+def _check_same_device(*ts):
+    dev = next(t.device for t in ts if t is not None)
+    for t in ts:
+        if t is not None and t.device != dev:
+            raise ValueError(f"all tensors of one call must be on one device ({dev}), got one on {t.device}")
+
+
+def _check_attention(q, k, v=None, o=None, lse=None, q_like=None, k_like=None):
+    """The library sees only pointers and sizes, so every tensor's shape and
+    dtype is checked against q (queries) and k (keys) here: a mismatch would
+    make a kernel read or write past a buffer.  ``v`` and the named tensors
+    of ``k_like`` are [B, H, Nk, d] like k; ``o`` and those of ``q_like``
+    [B, H, Nq, d] like q; ``lse``
+    float32 with B*H*Nq contiguous elements.  Shapes are checked first, then
+    that every tensor is on one CUDA device."""
+    B, H, Nq, d = _dims(q)
+    _, _, Nk, _ = _dims(k)
+    if k.dim() != q.dim() or tuple(_dims(k)) != (B, H, Nk, d):
+        raise ValueError(f"k has shape {tuple(k.shape)}; q {tuple(q.shape)} wants [B={B}, H={H}, Nk, d={d}]")
+    if k.dtype != q.dtype:
+        raise TypeError(f"k is {k.dtype}, q is {q.dtype}: one dtype per call")
+    q_like, k_like = dict(q_like or {}), dict(k_like or {})
+    for name, t, want in ([("v", v, (B, H, Nk, d))] + [(n, t, (B, H, Nk, d)) for n, t in k_like.items()] +
+                          [("o", o, (B, H, Nq, d))] + [(n, t, (B, H, Nq, d)) for n, t in q_like.items()]):
+        if t is None:
+            continue
+        if t.dim() != q.dim() or tuple(_dims(t)) != want:
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {want} in the layout of q")
+        if t.dtype != q.dtype:
+            raise TypeError(f"{name} is {t.dtype}, q is {q.dtype}: one dtype per call")
+    if lse is not None and (lse.dtype != torch.float32 or not lse.is_contiguous() or lse.numel() != B * H * Nq):
+        raise ValueError(f"lse must be a contiguous float32 tensor of B*H*Nq = {B * H * Nq} elements")
+    ts = (q, k, v, o, lse, *q_like.values(), *k_like.values())
+    _check_cuda(*ts)
+    _check_same_device(*ts)
+
+
 def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
            sm_scale: float, causal: bool, stream=None) -> None:
     """O and LSE of exact attention into the caller's ``o`` and ``lse``."""
-    _check_cuda(q, k, v, o, lse)
+    dt = _dtype_code(q)
+    _check_attention(q, k, v, o, lse)
     B, H, Nq, d = _dims(q)
     _, _, Nk, _ = _dims(k)
-    dt = _dtype_code(q)
-    if lse.dtype != torch.float32 or not lse.is_contiguous():
-        raise ValueError("lse must be a contiguous float32 tensor [B, H, Nq]")
     L = lib()
-    if all(_is_bhsd_contiguous(t) for t in (q, k, v, o)):
-        rc = L.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d, float(sm_scale),
-                      int(bool(causal)), dt, _stream(stream))
-    else:
-        lay = Layout()
-        lay.q, lay.k, lay.v, lay.o = _strides(q), _strides(k), _strides(v), _strides(o)
-        rc = L.fa_fwd_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d, float(sm_scale),
-                              int(bool(causal)), dt, ctypes.byref(lay), _stream(stream))
+    with torch.cuda.device(q.device):
+        if all(_is_bhsd_contiguous(t) for t in (q, k, v, o)):
+            rc = L.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d, float(sm_scale),
+                          int(bool(causal)), dt, _stream(stream, q.device))
+        else:
+            lay = Layout()
+            lay.q, lay.k, lay.v, lay.o = _strides(q), _strides(k), _strides(v), _strides(o)
+            rc = L.fa_fwd_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
+                                  float(sm_scale), int(bool(causal)), dt, ctypes.byref(lay),
+                                  _stream(stream, q.device))
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd")
 
@@ -221,7 +258,6 @@ def fa_fwd_fp8v(q: torch.Tensor, k: torch.Tensor, vt: torch.Tensor, o: torch.Ten
     (torch.float8_e5m2 or its raw uint8 codes) with unit stride along keys,
     ld = vt.stride(2) >= Nk and a multiple of 16; q, k, o contiguous
     [B, H, seq, d] fp16/bf16."""
-    _check_cuda(q, k, vt, o, lse)
     B, H, Nq, d = _dims(q)
     _, _, Nk, _ = _dims(k)
     dt = _dtype_code(q)
@@ -232,13 +268,15 @@ def fa_fwd_fp8v(q: torch.Tensor, k: torch.Tensor, vt: torch.Tensor, o: torch.Ten
     ld = vt.stride(2)
     if vt.stride(1) != d * ld or vt.stride(0) != H * d * ld:
         raise ValueError("vt rows must be packed: strides (H*d*ld, d*ld, ld, 1)")
-    if lse.dtype != torch.float32 or not lse.is_contiguous():
-        raise ValueError("lse must be a contiguous float32 tensor [B, H, Nq]")
+    _check_attention(q, k, None, o, lse)
+    _check_cuda(vt)
+    _check_same_device(q, vt)
     for t in (q, k, o):
         if not _is_bhsd_contiguous(t):
             raise ValueError("q, k and o must be contiguous [B, H, seq, d]")
-    rc = lib().fa_fwd_fp8v(_ptr(q), _ptr(k), _ptr(vt), _ptr(o), _ptr(lse), B, H, Nq, Nk, d, int(ld),
-                           float(sm_scale), int(bool(causal)), dt, _stream(stream))
+    with torch.cuda.device(q.device):
+        rc = lib().fa_fwd_fp8v(_ptr(q), _ptr(k), _ptr(vt), _ptr(o), _ptr(lse), B, H, Nq, Nk, d, int(ld),
+                               float(sm_scale), int(bool(causal)), dt, _stream(stream, q.device))
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd_fp8v")
 
@@ -257,21 +295,21 @@ def fa_fwd_split(q, k, v, o, lse, sm_scale: float, causal: bool, n_splits: int,
 
     ``workspace`` is a CUDA byte tensor of at least
     ``fa_fwd_split_workspace_bytes`` (unused when ``n_splits == 1``)."""
-    _check_cuda(q, k, v, o, lse)
+    dt = _dtype_code(q)
+    _check_attention(q, k, v, o, lse)
     B, H, Nq, d = _dims(q)
     _, _, Nk, _ = _dims(k)
-    dt = _dtype_code(q)
-    if lse.dtype != torch.float32 or not lse.is_contiguous():
-        raise ValueError("lse must be a contiguous float32 tensor [B, H, Nq]")
     ws_ptr, ws_bytes = None, 0
     if workspace is not None:
         _check_cuda(workspace)
+        _check_same_device(q, workspace)
         ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
     lay = Layout()
     lay.q, lay.k, lay.v, lay.o = _strides(q), _strides(k), _strides(v), _strides(o)
-    rc = lib().fa_fwd_split(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d, float(sm_scale),
-                            int(bool(causal)), dt, ctypes.byref(lay), int(n_splits), ws_ptr, ws_bytes,
-                            _stream(stream))
+    with torch.cuda.device(q.device):
+        rc = lib().fa_fwd_split(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d, float(sm_scale),
+                                int(bool(causal)), dt, ctypes.byref(lay), int(n_splits), ws_ptr, ws_bytes,
+                                _stream(stream, q.device))
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd_split")
 
@@ -288,26 +326,31 @@ def fa_bwd(q, k, v, o, do, lse, dq, dk, dv, sm_scale: float, causal: bool,
     if omitted, one is allocated here with torch (the library itself never
     allocates).
     """
-    _check_cuda(q, k, v, o, do, lse, dq, dk, dv, workspace)
+    dt = _dtype_code(q)
+    _check_attention(q, k, v, o, lse, q_like={"do": do, "dq": dq}, k_like={"dk": dk, "dv": dv})
+    if workspace is not None:
+        _check_cuda(workspace)
+        _check_same_device(q, workspace)
     B, H, Nq, d = _dims(q)
     _, _, Nk, _ = _dims(k)
-    dt = _dtype_code(q)
     need = fa_bwd_workspace_bytes(B, H, Nq, Nk, d)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     ws_bytes = workspace.numel() * workspace.element_size()
     L = lib()
     ts = (q, k, v, o, do, dq, dk, dv)
-    if all(_is_bhsd_contiguous(t) for t in ts):
-        rc = L.fa_bwd(*[_ptr(t) for t in (q, k, v, o, do, lse, dq, dk, dv)], B, H, Nq, Nk, d, float(sm_scale),
-                      int(bool(causal)), dt, _ptr(workspace), ws_bytes, _stream(stream))
-    else:
-        lay = Layout()
-        lay.q, lay.k, lay.v, lay.o = _strides(q), _strides(k), _strides(v), _strides(o)
-        lay.dout, lay.dq, lay.dk, lay.dv = _strides(do), _strides(dq), _strides(dk), _strides(dv)
-        rc = L.fa_bwd_strided(*[_ptr(t) for t in (q, k, v, o, do, lse, dq, dk, dv)], B, H, Nq, Nk, d,
-                              float(sm_scale), int(bool(causal)), dt, ctypes.byref(lay), _ptr(workspace),
-                              ws_bytes, _stream(stream))
+    with torch.cuda.device(q.device):
+        if all(_is_bhsd_contiguous(t) for t in ts):
+            rc = L.fa_bwd(*[_ptr(t) for t in (q, k, v, o, do, lse, dq, dk, dv)], B, H, Nq, Nk, d,
+                          float(sm_scale), int(bool(causal)), dt, _ptr(workspace), ws_bytes,
+                          _stream(stream, q.device))
+        else:
+            lay = Layout()
+            lay.q, lay.k, lay.v, lay.o = _strides(q), _strides(k), _strides(v), _strides(o)
+            lay.dout, lay.dq, lay.dk, lay.dv = _strides(do), _strides(dq), _strides(dk), _strides(dv)
+            rc = L.fa_bwd_strided(*[_ptr(t) for t in (q, k, v, o, do, lse, dq, dk, dv)], B, H, Nq, Nk, d,
+                                  float(sm_scale), int(bool(causal)), dt, ctypes.byref(lay), _ptr(workspace),
+                                  ws_bytes, _stream(stream, q.device))
     if rc != FA_OK:
         raise FaError(rc, "fa_bwd")
 
@@ -316,7 +359,10 @@ def fa_bwd_phase(phase: int, q, k, v, o, do, lse, dq, dk, dv, sm_scale: float, c
                  workspace: torch.Tensor, stream=None) -> None:
     """One of the three launches of fa_bwd (FA_BWD_PREPROCESS, FA_BWD_DKDV,
     FA_BWD_DQ); calling the three in order with one workspace equals fa_bwd."""
-    _check_cuda(q, k, v, o, do, lse, dq, dk, dv, workspace)
+    dt = _dtype_code(q)
+    _check_attention(q, k, v, o, lse, q_like={"do": do, "dq": dq}, k_like={"dk": dk, "dv": dv})
+    _check_cuda(workspace)
+    _check_same_device(q, workspace)
     B, H, Nq, d = _dims(q)
     _, _, Nk, _ = _dims(k)
     ts = (q, k, v, o, do, dq, dk, dv)
@@ -325,10 +371,11 @@ def fa_bwd_phase(phase: int, q, k, v, o, do, lse, dq, dk, dv, sm_scale: float, c
         lay = Layout()
         lay.q, lay.k, lay.v, lay.o = _strides(q), _strides(k), _strides(v), _strides(o)
         lay.dout, lay.dq, lay.dk, lay.dv = _strides(do), _strides(dq), _strides(dk), _strides(dv)
-    rc = lib().fa_bwd_phase(int(phase), *[_ptr(t) for t in (q, k, v, o, do, lse, dq, dk, dv)], B, H, Nq, Nk, d,
-                            float(sm_scale), int(bool(causal)), _dtype_code(q),
-                            None if lay is None else ctypes.byref(lay), _ptr(workspace),
-                            workspace.numel() * workspace.element_size(), _stream(stream))
+    with torch.cuda.device(q.device):
+        rc = lib().fa_bwd_phase(int(phase), *[_ptr(t) for t in (q, k, v, o, do, lse, dq, dk, dv)], B, H, Nq, Nk,
+                                d, float(sm_scale), int(bool(causal)), dt,
+                                None if lay is None else ctypes.byref(lay), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _stream(stream, q.device))
     if rc != FA_OK:
         raise FaError(rc, f"fa_bwd_phase({phase})")
 
@@ -344,22 +391,26 @@ def fa_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, sm_scale: float, causal: boo
     (B*H*ceil(Nq/128)*128 > 2,097,152 rows) raise FaError(FA_ERR_WORKSPACE).
     Calls that can overlap on the GPU share that array and race: serialise
     them.  Contiguous [B, H, seq, d] tensors only."""
-    _check_cuda(q, k, v, o, do, lse, dq, dk, dv)
+    dt = _dtype_code(q)
+    _check_attention(q, k, v, o, lse, q_like={"do": do, "dq": dq}, k_like={"dk": dk, "dv": dv})
     ts = (q, k, v, o, do, dq, dk, dv)
     if not all(_is_bhsd_contiguous(t) for t in ts):
         raise ValueError("fa_bwd_noalloc takes contiguous [B, H, seq, d] tensors")
     B, H, Nq, d = _dims(q)
     _, _, Nk, _ = _dims(k)
-    rc = lib().fa_bwd_noalloc(*[_ptr(t) for t in (q, k, v, o, do, lse, dq, dk, dv)], B, H, Nq, Nk, d,
-                              float(sm_scale), int(bool(causal)), _dtype_code(q), _stream(stream))
+    with torch.cuda.device(q.device):
+        rc = lib().fa_bwd_noalloc(*[_ptr(t) for t in (q, k, v, o, do, lse, dq, dk, dv)], B, H, Nq, Nk, d,
+                                  float(sm_scale), int(bool(causal)), dt, _stream(stream, q.device))
     if rc != FA_OK:
         raise FaError(rc, "fa_bwd_noalloc")
 
 
-def fa_last_device_error(stream=None) -> Tuple[int, int]:
-    """(status, raw device code); synchronises the stream."""
+def fa_last_device_error(stream=None, device=None) -> Tuple[int, int]:
+    """(status, raw device code) of ``device`` (default: the current one);
+    synchronises the stream."""
     detail = ctypes.c_int(0)
-    rc = lib().fa_last_device_error(_stream(stream), ctypes.byref(detail))
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        rc = lib().fa_last_device_error(_stream(stream, device), ctypes.byref(detail))
     return rc, detail.value
 
 
@@ -401,9 +452,10 @@ def fa_softmax_rows(x: torch.Tensor, z: torch.Tensor, lse: Optional[torch.Tensor
     """Row softmax of the 2-D CUDA tensor ``x`` ([rows, T], unit column
     stride) into ``z`` (same shape and dtype; may be ``x`` itself), and the
     natural-log row log-sum-exp into the float32 [rows] ``lse`` if given."""
-    _check_cuda(x, z, lse)
     if x.dim() != 2 or z.shape != x.shape or z.dtype != x.dtype:
         raise ValueError("x and z must be 2-D tensors of the same shape and dtype")
+    _check_cuda(x, z, lse)
+    _check_same_device(x, z, lse)
     if x.dtype not in _SOFTMAX_DTYPES:
         raise TypeError(f"unsupported dtype {x.dtype} (float32, float16 or bfloat16)")
     if x.stride(1) != 1 or z.stride(1) != 1:
@@ -413,8 +465,9 @@ def fa_softmax_rows(x: torch.Tensor, z: torch.Tensor, lse: Optional[torch.Tensor
         raise ValueError("lse must be a contiguous float32 tensor of `rows` elements")
     # a single row's stride is never used: give the smallest valid one
     one = -(-T * x.element_size() // 16) * 16 // x.element_size()
-    rc = lib().fa_softmax_rows(_ptr(x), _ptr(z), _ptr(lse) if lse is not None else None, rows, T,
-                               x.stride(0) if rows > 1 else one, z.stride(0) if rows > 1 else one,
-                               _SOFTMAX_DTYPES[x.dtype], _stream(stream))
+    with torch.cuda.device(x.device):
+        rc = lib().fa_softmax_rows(_ptr(x), _ptr(z), _ptr(lse) if lse is not None else None, rows, T,
+                                   x.stride(0) if rows > 1 else one, z.stride(0) if rows > 1 else one,
+                                   _SOFTMAX_DTYPES[x.dtype], _stream(stream, x.device))
     if rc != FA_OK:
         raise FaError(rc, "fa_softmax_rows")
