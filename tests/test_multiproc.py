@@ -68,3 +68,25 @@ def test_single_process_defaults():
     assert bench.dist_init("gloo") == (0, 1)
     assert bench.reduce_max(3.5) == 3.5
     bench.barrier()   # a no-op without a process group
+
+
+@pytest.mark.timeout(300)
+def test_reference_arm_under_torchrun_prints_once():
+    """`bench.py --impl reference` launched the way N > 1 runs are (torchrun,
+    two ranks, gloo on CPU): rank 0 alone times the oracle and prints one JSON
+    line; the other rank exits 0 without work."""
+    import json
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), os.path.join(root, "bench.py"),
+           "--impl", "reference", "--gpus", "2", "--workload", "bf16_b4_h12_n512_d64_causal", "--steps", "1",
+           "--warmup", "3"]
+    out = subprocess.run(cmd, capture_output=True, text=True, timeout=240, cwd=root)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, out.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
