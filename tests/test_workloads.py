@@ -36,3 +36,24 @@ def test_flop_accounting():
     assert w.bwd_flops() == 2.5 * w.fwd_flops()
     w2 = W.custom("fp16", "shd", 1, 16, 1000, 2500, 80, False)
     assert w2.fwd_flops() == 4 * 16 * 1000 * 2500 * 80
+
+
+def test_fp8v_inputs_layout_and_padding():
+    import numpy as np
+
+    import oracle.fp8 as ref8
+
+    w = W.custom("fp16", "bhsd", 2, 3, 40, 70, 64, True, seed=5)
+    x = W.fp8v_inputs(w, ld=96, pad_code=0x7F)
+    vt, v8 = x["vt"], x["v8"]
+    assert vt.dtype == torch.uint8 and vt.shape == (2, 3, 64, 96)
+    assert v8.shape == (2, 3, 70, 64) and v8.dtype == torch.float32
+    assert torch.all(vt[..., 70:] == 0x7F)                       # bytes past Nk hold the pad code
+    # vt[b, h, c, j] is the e5m2 code of v8[b, h, j, c]
+    dec = ref8.e5m2_decode(vt[..., :70].numpy())
+    assert np.array_equal(dec, v8.transpose(-1, -2).numpy().astype(np.float64))
+    # the codes are V of make_inputs rounded to e5m2: within the format's 2^-3 relative step
+    v = W.make_inputs(w)["v"].float()
+    assert torch.all((v8 - v).abs() <= 2.0 ** -3 * v.abs() + 2.0 ** -17)
+    # default row length: Nk rounded up to 16
+    assert W.fp8v_inputs(w)["vt"].shape[-1] == 80
