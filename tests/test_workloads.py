@@ -57,3 +57,17 @@ def test_fp8v_inputs_layout_and_padding():
     assert torch.all((v8 - v).abs() <= 2.0 ** -3 * v.abs() + 2.0 ** -17)
     # default row length: Nk rounded up to 16
     assert W.fp8v_inputs(w)["vt"].shape[-1] == 80
+
+
+def test_algorithmic_bytes_match_the_configuration_table():
+    # fwd: q, k, v read and o written once (2 bytes each) plus the fp32 LSE;
+    # bwd: q, k, v, o, dO read and dq, dk, dv written, plus LSE and D per row
+    mb = {n: W.WORKLOADS[n].fwd_bytes() / 1e6 for n in W.WORKLOADS}
+    assert abs(mb["fp16_h16_nq1000_nk2500_d80"] - 17.98) < 0.01
+    assert abs(mb["bf16_b4_h12_n512_d64_causal"] - 12.68) < 0.01
+    assert abs(mb["bf16_b4_h20_n4096_d64_causal"] - 169.08) < 0.01
+    assert abs(mb[W.BENCH_WORKLOAD] - 675.28) < 0.01
+    assert abs(W.WORKLOADS[W.BENCH_WORKLOAD].bwd_bytes() / 1e9 - 1.3506) < 1e-4
+    # the causal mask halves the work, not the bytes
+    w = W.custom("bf16", "bhsd", 1, 1, 256, 256, 64, True)
+    assert w.fwd_bytes() == W.custom("bf16", "bhsd", 1, 1, 256, 256, 64, False).fwd_bytes()
