@@ -20,9 +20,14 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  * - All tensor pointers are DEVICE pointers owned by the caller.  The library
- *   never allocates, frees or keeps device memory of its own apart from one
- *   4-byte error word per device.  Outputs are fully overwritten (no
- *   accumulate-into semantics), so they need no zeroing.
+ *   never allocates or frees device memory.  It keeps two statically sized
+ *   device arrays in every GPU that loads it: one 4-byte error word, and the
+ *   16 MiB scratch array that only fa_bwd_noalloc uses (below).  Outputs are
+ *   fully overwritten (no accumulate-into semantics), so they need no zeroing.
+ * - The device addresses of those arrays are looked up once per device, on
+ *   the first call that needs them, and kept for the life of the process:
+ *   resetting a device (cudaDeviceReset) after that first call is not
+ *   supported.
  * - Element type: FA_FP16 or FA_BF16 for Q, K, V, O, dO, dQ, dK, dV; the
  *   log-sum-exp is always float32.  Arithmetic is fp32 accumulation on the
  *   tensor cores, P and dS are rounded to the input type before their GEMMs.
@@ -186,7 +191,9 @@ FA_API fa_status fa_fwd_fp8v(const void* q, const void* k, const void* vt, void*
 /*
  * fa_bwd_workspace_bytes -- size of the scratch buffer fa_bwd needs: the
  * per-row D = rowsum(O o dO) and the log2-domain LSE, float32, padded to
- * whole 128-row query tiles: 2 * 4 * B*H*ceil(Nq/128)*128 bytes.
+ * whole 128-row query tiles: 2 * 4 * B*H*ceil(Nq/128)*128 bytes.  ("[CS336]",
+ * "FlashAttention V2 / Backward Pass": D is computed once, before the two
+ * passes, and kept in global memory.)
  */
 FA_API size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int Nk, int d);
 
@@ -206,7 +213,10 @@ FA_API fa_status fa_bwd(const void* q, const void* k, const void* v, const void*
                  int B, int H, int Nq, int Nk, int d, float sm_scale, int causal,
                  fa_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
 
-/* fa_bwd with explicit strides (layout->q, k, v, o, dout, dq, dk, dv). */
+/* fa_bwd with explicit strides (layout->q, k, v, o, dout, dq, dk, dv), e.g.
+ * the [seq, heads, d] layout of "BUG in flash attention kernel".  Every
+ * tensor is addressed with its own strides: the kernel in that issue offset
+ * K and V by Q's head stride, which is wrong once Nq != Nk. */
 FA_API fa_status fa_bwd_strided(const void* q, const void* k, const void* v, const void* o, const void* dout,
                          const float* lse, void* dq, void* dk, void* dv,
                          int B, int H, int Nq, int Nk, int d, float sm_scale, int causal,
@@ -263,7 +273,6 @@ FA_API fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, con
                          int B, int H, int Nq, int Nk, int d, float sm_scale, int causal,
                          fa_dtype dtype, void* stream);
 
-/* Human-readable name of a status code (static string, never NULL). */
 /*
  * fa_softmax_rows -- row-wise softmax of a [rows, T] matrix with the online
  * max/sum recurrence ("Puzzles 8 Long Softmax": z_ij = softmax_j(x_i1..x_iT),
@@ -288,10 +297,14 @@ FA_API fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, con
 FA_API fa_status fa_softmax_rows(const void* x, void* z, float* lse, int rows, int T, int64_t x_row_stride,
                           int64_t z_row_stride, fa_dtype dtype, void* stream);
 
+/* Human-readable name of a status code (static string, never NULL); codes
+ * outside fa_status give "unknown fa_status".  Library plumbing: the pages
+ * have no counterpart. */
 FA_API const char* fa_status_string(fa_status status);
 
 /*
- * fa_last_device_error -- synchronises `stream`, then reads and clears the
+ * fa_last_device_error -- (library plumbing; the pages have no counterpart)
+ * synchronises `stream`, then reads and clears the
  * current device's error word.  Returns FA_ERR_TIMEOUT if a kernel gave up a
  * bounded wait since the last call, FA_ERR_CUDA if the synchronisation
  * failed, else FA_OK.  *detail (if non-NULL) receives the raw device code

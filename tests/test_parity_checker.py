@@ -1,0 +1,145 @@
+"""The backward parity checker (tests/parity.py) accepts what a correct
+kernel returns and rejects planted mistakes, on the CPU.
+
+A correct result is stood in for by the float64 oracle's gradients rounded to
+the input type (what a kernel without any error of its own would return) and
+by the same-precision naive reference itself.  Each mistake is planted into a
+copy of the rounded oracle gradients.  The mistakes include the one the
+per-head bound alone cannot see: zeroing the rows whose gradients are small
+next to the head's largest (in a long causal bf16 head a sizable share of
+dV's rows lies wholly below 1e-2 x max |dV|).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.attention as ref
+from tiled_attention_07_gb300 import workloads as W
+
+from parity import GRAD_TOL, check_grads, half_ulp, naive_grads
+
+CASES = [
+    # dtype, Nq, Nk, d, causal, std
+    ("bf16", 1024, 1024, 80, True, 1.0),
+    ("fp16", 300, 700, 64, False, 0.5),
+    ("bf16", 640, 256, 128, True, 1.0),
+]
+
+
+def _setup(case):
+    dtype, nq, nk, d, causal, std = case
+    w = W.custom(dtype, "bhsd", 1, 1, nq, nk, d, causal, std=std, seed=nq + nk + d, backward=True)
+    x = W.make_inputs(w)
+    q, k, v, do = (x[n][0, 0].double().numpy() for n in ("q", "k", "v", "do"))
+    dq, dk, dv, _ = ref.backward(q, k, v, do, w.sm_scale, w.causal)
+    exact = {"dq": dq, "dk": dk, "dv": dv}
+    naive = dict(zip(("dq", "dk", "dv"), naive_grads(q, k, v, do, w.sm_scale, w.causal, w.dtype)))
+    rounded = {n: torch.from_numpy(a).to(w.torch_dtype).double().numpy() for n, a in exact.items()}
+    return w, exact, naive, rounded
+
+
+def _round(a, dtype):
+    return torch.from_numpy(a).to(W.DTYPES[dtype]).double().numpy()
+
+
+def _per_head_bound_only(dtype, got, exact):
+    """The per-head bound (a) on its own: True if it accepts `got`."""
+    for n in ("dq", "dk", "dv"):
+        r = exact[n]
+        excess = (np.abs(got[n] - r) - half_ulp(r, dtype)) / max(1.0, float(np.abs(r).max()))
+        if excess.max() > GRAD_TOL[dtype]:
+            return False
+    return True
+
+
+@pytest.fixture(scope="module", params=CASES, ids=["-".join(map(str, c)) for c in CASES])
+def setup(request):
+    return _setup(request.param)
+
+
+def test_correct_results_pass(setup):
+    w, exact, naive, rounded = setup
+    stats = {}
+    check_grads(w.dtype, rounded, exact, naive, "rounded oracle", stats)
+    check_grads(w.dtype, naive, exact, naive, "naive", stats)
+    # the rounded exact result sits well inside the bound
+    assert max(stats[f"max_row_ratio_{n}"] for n in ("dq", "dk", "dv")) < 1.0, stats
+
+
+def _rows_below_head_tolerance(dtype, a):
+    """Rows whose every element lies below the per-head bound (a): zeroing
+    them is invisible to that bound."""
+    lim = GRAD_TOL[dtype] * max(1.0, float(np.abs(a).max()))
+    rows = np.abs(a).max(axis=1) < lim
+    return rows & (np.abs(a).max(axis=1) > 0)
+
+
+def _mutants(w, g):
+    """(name, mutated copy of g) pairs; g holds the rounded oracle gradients."""
+    nk = g["dv"].shape[0]
+    out = []
+    m = {n: a.copy() for n, a in g.items()}
+    m["dv"][nk // 2:] = 0.0
+    out.append(("dV rows >= Nk/2 zeroed", m))
+    m = {n: a.copy() for n, a in g.items()}
+    t0 = min(128, nk - 1)
+    m["dk"][t0:t0 + 128] = _round(m["dk"][t0:t0 + 128] * 1.01, w.dtype)
+    out.append(("dK 1 % high on one key tile", m))
+    below = _rows_below_head_tolerance(w.dtype, g["dv"])
+    if below.any():   # rows that small occur in long causal heads
+        m = {n: a.copy() for n, a in g.items()}
+        m["dv"][below] = 0.0
+        out.append(("the dV rows below the per-head tolerance zeroed", m))
+    m = {n: a.copy() for n, a in g.items()}
+    r = int(np.argmax(np.linalg.norm(m["dq"], axis=1)))
+    c = int(np.argmax(np.abs(m["dq"][r])))
+    m["dq"][r, c] = -m["dq"][r, c]
+    out.append(("one dQ element with its sign flipped", m))
+    m = {n: a.copy() for n, a in g.items()}
+    m["dk"][[5, 6]] = m["dk"][[6, 5]]
+    out.append(("two adjacent dK rows swapped", m))
+    m = {n: a.copy() for n, a in g.items()}
+    m["dq"] = _round(m["dq"] * 0.995, w.dtype)
+    out.append(("dQ 0.5 % low everywhere", m))
+    return out
+
+
+def test_planted_mistakes_are_rejected(setup):
+    w, exact, naive, rounded = setup
+    for name, m in _mutants(w, rounded):
+        with pytest.raises(AssertionError):
+            check_grads(w.dtype, m, exact, naive, name, {})
+
+
+def test_small_rows_zeroed_pass_the_per_head_bound_alone():
+    # Why the per-row bound exists: on a long causal bf16 head, a sizable
+    # share of dV's rows lies wholly below the per-head tolerance, and zeroing
+    # all of them stays inside that bound.
+    w, exact, naive, rounded = _setup(("bf16", 2048, 2048, 80, True, 1.0))
+    share = _rows_below_head_tolerance(w.dtype, rounded["dv"]).mean()
+    assert share > 0.1, share
+    name, m = _mutants(w, rounded)[2]
+    assert name.startswith("the dV rows below")
+    assert _per_head_bound_only(w.dtype, m, exact)
+    with pytest.raises(AssertionError, match="dv row"):
+        check_grads(w.dtype, m, exact, naive, name, {})
+
+
+def test_naive_reference_follows_the_definition():
+    # Pinned apart from the GPU: in float64, without the roundings, the naive
+    # steps give the oracle's gradients; its error at the storage precision is
+    # of the order of the output rounding (a few 2^-9 per row in bf16).
+    w, exact, naive, rounded = _setup(("bf16", 256, 384, 64, True, 1.0))
+    for n in ("dq", "dk", "dv"):
+        rel = np.linalg.norm(naive[n] - exact[n], axis=1) / np.maximum(np.linalg.norm(exact[n], axis=1), 1e-30)
+        live = np.linalg.norm(exact[n], axis=1) > 1e-6
+        assert np.median(rel[live]) < 4 * 2.0 ** -9, (n, np.median(rel[live]))
+    nf = dict(zip(("dq", "dk", "dv"), naive_grads(*_f64_inputs(w), w.sm_scale, w.causal, "fp32")))
+    for n in ("dq", "dk", "dv"):
+        np.testing.assert_allclose(nf[n], exact[n], rtol=0, atol=1e-5 * max(1.0, np.abs(exact[n]).max()))
+
+
+def _f64_inputs(w):
+    x = W.make_inputs(w)
+    return tuple(x[n][0, 0].double().numpy() for n in ("q", "k", "v", "do"))

@@ -24,6 +24,11 @@ from parity import GRAD_TOL, half_ulp, to64
 
 
 def test_oversized_problem_is_refused_before_launch():
+    # The pointers below are fake device addresses.  Should the size check
+    # ever let one through, a launch would follow, so this runs only where no
+    # GPU is visible.
+    if torch.cuda.is_available():
+        pytest.skip("fake device addresses: the size check runs on a machine without a GPU")
     if not os.path.exists(fa.LIB_PATH):
         from tiled_attention_07_gb300 import build
         build.build()
@@ -73,3 +78,46 @@ def test_noalloc_matches_fa_bwd_on_two_calls_in_a_row():
             scale = max(1.0, float(np.abs(b64).max()))
             excess = (np.abs(a64 - b64) - half_ulp(b64, w.dtype)) / scale
             assert excess.max() <= tol, (w.name, name, float(excess.max()))
+
+
+@pytest.mark.gpu
+def test_noalloc_at_the_scratch_limit_allocates_nothing():
+    # Exactly FA_NOALLOC_SCRATCH_BYTES of scratch: 16 heads of 131,072 query
+    # rows (2,097,152 padded rows), where the entry point's own size check and
+    # the backward's workspace check must agree.  Nk is one key tile, so the
+    # problem stays small in time.
+    rows = fa.NOALLOC_SCRATCH_BYTES // 8
+    w = W.custom("bf16", "bhsd", 2, 8, rows // 16, 128, 64, False, seed=73, backward=True)
+    assert fa.fa_bwd_workspace_bytes(w.B, w.H, w.Nq, w.Nk, w.d) == fa.NOALLOC_SCRATCH_BYTES
+    x = W.make_inputs(w, device="cuda")
+    o, lse = fa.attention_forward(x["q"], x["k"], x["v"], w.sm_scale, w.causal)
+    want = _reference_grads(w, x, o, lse)
+    dq, dk, dv = (torch.full_like(t, float("nan")) for t in (x["q"], x["k"], x["v"]))
+    stream = torch.cuda.current_stream().cuda_stream
+    L = fa.lib()
+
+    def call():
+        return L.fa_bwd_noalloc(x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(), o.data_ptr(),
+                                x["do"].data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                w.B, w.H, w.Nq, w.Nk, w.d, w.sm_scale, int(w.causal), fa.FA_BF16, stream)
+
+    assert call() == fa.FA_OK   # warm-up: kernels loaded, scratch address looked up
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    alloc0 = torch.cuda.memory_allocated()
+    dq.fill_(float("nan"))
+    dk.fill_(float("nan"))
+    dv.fill_(float("nan"))
+    assert call() == fa.FA_OK
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert torch.cuda.memory_allocated() == alloc0
+    assert free1 == free0, (free0, free1)
+    rc, detail = fa.fa_last_device_error()
+    assert rc == fa.FA_OK, f"device error {detail:#x}"
+    for name, a, b in zip(("dq", "dk", "dv"), (dq, dk, dv), want):
+        assert torch.equal(a, b), name
+    # one query tile more is refused before anything runs
+    assert L.fa_bwd_noalloc(x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(), o.data_ptr(),
+                            x["do"].data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                            w.B, w.H, w.Nq + 1, w.Nk, w.d, w.sm_scale, 0, fa.FA_BF16, stream) == fa.FA_ERR_WORKSPACE
