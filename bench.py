@@ -48,6 +48,9 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the forward-only timing of the other configurations (the 'configs' key)")
+    ap.add_argument("--config-steps", type=int, default=50, help="timed forwards per configuration in 'configs'")
     ap.add_argument("--fwd-only", action="store_true",
                     help="time only the forward of --workload (the forward-only configurations), one JSON line")
     ap.add_argument("--split", default="1", help="with --fwd-only: key-range splits (an integer, or 'auto')")
@@ -153,6 +156,30 @@ def load_peaks():
         return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
     except (OSError, KeyError, ValueError):
         return dict(FALLBACK_PEAKS), "fallback"
+
+
+#: Dense bf16 tensor-core peak of one GB300 on paper (context next to the
+#: measured figure).
+NOMINAL_BF16_TFLOPS = 2250.0
+
+
+def tensor_peak(peaks, peak_src, clk):
+    """The bf16 tensor peak that kernels timed in this run are held against.
+
+    The measured burst figure (a cuBLAS GEMM timed alone at full clock): every
+    timed region of this bench lasts well under a second, and the clocks
+    sampled during it show whether the SMs stayed at full clock.  If the
+    median sampled SM clock fell below 95 % of the maximum, the burst figure
+    is scaled by that ratio (tensor throughput follows the SM clock).  The
+    sustained figure was measured at a clock far below the maximum under a
+    seconds-long GEMM loop, which these kernels never see."""
+    burst = peaks["bf16_tflops"]
+    mhz = clk.get("sm_mhz") if clk else None
+    mx = clk.get("sm_max_mhz") if clk else None
+    if mhz and mx and mhz < 0.95 * mx:
+        return round(burst * mhz / mx, 1), (f"{peak_src} bf16 burst x median sampled SM clock "
+                                            f"({mhz:.0f} of {mx:.0f} MHz)")
+    return burst, f"{peak_src} bf16 burst (timed region well under a second, SMs at full clock)"
 
 
 #: Sources each kernel is compiled from (a change to any of them makes an
@@ -293,7 +320,7 @@ def run_ours(args):
     value = world * K * step_flops / (ms / 1e3) / 1e12
     kern_ms = {n: sum(e[j].elapsed_time(e[j + 1]) for e in evs) / K for j, n in enumerate(names)}
     peaks, peak_src = load_peaks()
-    peak = peaks["bf16_tflops_sustained"]
+    peak, peak_note = tensor_peak(peaks, peak_src, clk)
     kflops = per_kernel_flops(w)
     kernels = {}
     for n in names:
@@ -305,13 +332,17 @@ def run_ours(args):
     dom = max((n for n in names if kflops[n] > 0), key=lambda n: kern_ms[n])
     achieved = kflops[dom] / (kern_ms[dom] / 1e3) / 1e12
     roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(achieved / peak, 4), "traffic": committed_traffic(dom),
-                "peak_source": f"{peak_src} bf16 sustained (kernel timed inside back-to-back steps)"}
+                "frac": round(achieved / peak, 4), "traffic": committed_traffic(dom), "peak_source": peak_note,
+                "frac_of_nominal": round(achieved / NOMINAL_BF16_TFLOPS, 4)}
     fwd_tf = w.fwd_flops() / (kern_ms["fwd"] / 1e3) / 1e12
     bwd_ms = kern_ms["bwd_pre"] + kern_ms["bwd_dkdv"] + kern_ms["bwd_dq"]
     bwd_tf = w.bwd_flops() / (bwd_ms / 1e3) / 1e12
-    passes = {"fwd": {"tflops": round(fwd_tf, 2), "frac_of_peak": round(fwd_tf / peak, 4)},
-              "bwd": {"tflops_credited": round(bwd_tf, 2), "frac_of_peak": round(bwd_tf / peak, 4)}}
+    passes = {"fwd": {"tflops": round(fwd_tf, 2), "frac_of_peak": round(fwd_tf / peak, 4),
+                      "frac_of_nominal": round(fwd_tf / NOMINAL_BF16_TFLOPS, 4)},
+              "bwd": {"tflops_credited": round(bwd_tf, 2), "frac_of_peak": round(bwd_tf / peak, 4),
+                      "frac_of_nominal": round(bwd_tf / NOMINAL_BF16_TFLOPS, 4)},
+              "step": {"tflops": round(value / world, 2), "frac_of_peak": round(value / world / peak, 4),
+                       "frac_of_nominal": round(value / world / NOMINAL_BF16_TFLOPS, 4)}}
 
     e2e = None
     if not args.no_e2e:
@@ -319,6 +350,9 @@ def run_ours(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, host)
+    configs = None
+    if rank == 0 and not args.no_configs:
+        configs = run_configs(args, dev, peaks, peak_src)
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
@@ -332,10 +366,123 @@ def run_ours(args):
                    f"{q.numel() * 2 / 1e6:.0f} MB > 129 MB)", "parallelism": f"replica x{world}"},
         "roofline": roofline, "kernels": kernels, "passes": passes,
         "clocks": clk, "gpu_launches": 4 * K,
-        "e2e": e2e, "cpu_baseline": cpu,
+        "e2e": e2e, "cpu_baseline": cpu, "configs": configs,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+#: The forward-only configurations, timed after the step for the 'configs'
+#: key: the one-head smoke shape, the cross-attention shape, and the short
+#: and long causal d = 64 shapes.
+FORWARD_CONFIGS = (
+    ("C1", "fp16_h1_n128_d64"),
+    ("C2", "fp16_h16_nq1000_nk2500_d80"),
+    ("C3", "bf16_b4_h12_n512_d64_causal"),
+    ("C4", "bf16_b4_h20_n4096_d64_causal"),
+)
+
+
+def time_forward(fwd, stream, steps, warmup, flush):
+    """Mean device time (ms) of `fwd()` over `steps` calls, each bracketed by
+    CUDA events on `stream`; with `flush` (a buffer larger than L2) written
+    between calls, outside the events, so every call starts from a cold L2."""
+    import torch
+
+    for _ in range(max(warmup, 3)):
+        fwd()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        if flush is not None:
+            flush.fill_(i & 255)
+        evs[i][0].record(stream)
+        fwd()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs) / steps
+
+
+def forward_roofline(w, ms, peaks, tensor_peak_tflops, fbytes=None):
+    """TFLOP/s and GB/s of the algorithmic work of one forward of `w` in `ms`,
+    and its fraction of the roofline that bounds it: HBM when the arithmetic
+    intensity lies below the measured ridge (tensor peak / HBM bandwidth),
+    the tensor peak otherwise."""
+    flops = w.fwd_flops()
+    fbytes = w.fwd_bytes() if fbytes is None else fbytes
+    tflops = flops / (ms / 1e3) / 1e12
+    gbs = fbytes / (ms / 1e3) / 1e9
+    hbm = flops / fbytes < tensor_peak_tflops * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    return {"tflops": round(tflops, 2), "gbs": round(gbs, 1), "bound": "hbm" if hbm else "tensor",
+            "frac": round(gbs / peaks["hbm_gbs"] if hbm else tflops / tensor_peak_tflops, 4),
+            "peak": peaks["hbm_gbs"] if hbm else tensor_peak_tflops, "unit": "GB/s" if hbm else "TFLOP/s",
+            "intensity_flop_per_byte": round(flops / fbytes, 1)}
+
+
+def run_configs(args, dev, peaks, peak_src):
+    """Forward alone on each forward-only configuration, in this process and
+    on this GPU: ms per forward (mean of --config-steps), TFLOP/s, GB/s of the
+    algorithmic bytes and the fraction of the bounding roofline; inputs under
+    256 MB are made cold by a 256 MB write between forwards.  Next to each,
+    the oracle's forward on a bounded sample of the same configuration."""
+    import torch
+
+    from tiled_attention_07_gb300 import fa
+    from tiled_attention_07_gb300 import workloads as W
+
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    clocks = ClockSampler()
+    clocks.start()
+    time.sleep(0.3)
+    out = {}
+    hosts = {}
+    for cid, name in FORWARD_CONFIGS:
+        w = W.WORKLOADS[name]
+        host = W.make_inputs(w, device="cpu", with_grad_output=False)
+        hosts[cid] = host
+        x = {k: t.to(dev) for k, t in host.items()}
+        o = torch.empty_like(x["q"])
+        lse = torch.empty(fa.lse_shape(x["q"]), dtype=torch.float32, device=dev)
+        in_bytes = sum(t.numel() * t.element_size() for t in x.values())
+
+        def fwd(x=x, o=o, lse=lse, w=w):
+            fa.fa_fwd(x["q"], x["k"], x["v"], o, lse, w.sm_scale, w.causal, stream)
+
+        ms = time_forward(fwd, stream, args.config_steps, 10, flush if in_bytes < (256 << 20) else None)
+        rc, detail = fa.fa_last_device_error(stream)
+        if rc != fa.FA_OK:
+            raise RuntimeError(f"device error in {name}: {detail:#x}")
+        out[cid] = {"workload": name, "ms": round(ms, 5), "steps": args.config_steps, "launches": args.config_steps,
+                    "l2": "256 MB write between forwards" if in_bytes < (256 << 20) else "inputs larger than L2"}
+        out[cid]["_ms"] = ms
+        del x, o, lse
+    clk = clocks.stop()
+    tpeak, tnote = tensor_peak(peaks, peak_src, clk)
+    for cid, name in FORWARD_CONFIGS:
+        w = W.WORKLOADS[name]
+        ms = out[cid].pop("_ms")
+        out[cid].update(forward_roofline(w, ms, peaks, tpeak))
+        if not args.no_cpu_baseline:
+            out[cid]["cpu_baseline"] = cpu_forward_baseline(w, hosts[cid])
+    out["clocks"] = clk
+    out["tensor_peak_source"] = tnote
+    out["hbm_peak_source"] = f"{peak_src} HBM copy bandwidth"
+    return out
+
+
+def cpu_forward_baseline(w, host):
+    """The oracle's forward, as it stands, on head (0, 0) of `w` (the whole
+    problem when it has one head)."""
+    import oracle.attention as ref
+
+    q, k, v = (_head64(host[n], w.layout, 0, 0) for n in ("q", "k", "v"))
+    t = time.perf_counter()
+    ref.forward(q, k, v, w.sm_scale, w.causal)
+    sec = time.perf_counter() - t
+    pairs = w.Nq * w.Nk * (0.5 if w.causal else 1.0)
+    return {"value": round(4.0 * pairs * w.d / sec / 1e12, 6), "unit": "TFLOP/s", "cores": _cores(),
+            "kind": "oracle", "sample": f"forward of head (0,0) of {w.name} in float64 numpy, {sec:.3f} s"}
 
 
 def run_fwd_only(args):
@@ -411,14 +558,13 @@ def run_fwd_only(args):
     flops = w.fwd_flops()
     value = world * flops / (ms_step / 1e3) / 1e12
     peaks, peak_src = load_peaks()
-    peak = peaks["bf16_tflops"]
-    peak_note = f"{peak_src} bf16 burst (kernel timed alone)"
+    peak, peak_note = tensor_peak(peaks, peak_src, clk)
     if args.fp8v:
         # Half the FLOPs (S = q k^T) at the 16-bit rate P, half (P V) at the
         # 8-bit rate, taken as 2 P (the nominal fp8 : bf16 ratio): time at
         # peak F/2 (1/P + 1/(2P)), i.e. an effective peak of 4P/3.
         peak = round(peak * 4.0 / 3.0, 1)
-        peak_note = f"{peak_src} bf16 burst x 4/3: S at the 16-bit rate, PV at 2x (nominal fp8:bf16 ratio)"
+        peak_note += " x 4/3: S at the 16-bit rate, PV at 2x (nominal fp8:bf16 ratio)"
     # Bound by arithmetic intensity against the measured ridge: below it the
     # forward is an HBM stream and is reported as GB/s of its algorithmic bytes.
     fbytes = w.fwd_bytes() - (w.Nk * w.d * w.B * w.H if args.fp8v else 0)   # e5m2 V: one byte per element

@@ -42,3 +42,28 @@ def test_committed_traffic_follows_the_sources(monkeypatch):
         assert bench.committed_traffic(k) > 0, k   # the table matches the committed sources
     monkeypatch.setattr(bench, "kernel_source_hash", lambda kernel: "0000000000000000")
     assert bench.committed_traffic("bwd_dkdv") is None
+
+
+def test_tensor_peak_is_the_burst_figure_at_full_clock():
+    peaks = {"hbm_gbs": 6787.6, "bf16_tflops": 1887.4, "bf16_tflops_sustained": 1720.8}
+    p, note = bench.tensor_peak(peaks, "measured", {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0})
+    assert p == 1887.4 and "burst" in note
+    p, _ = bench.tensor_peak(peaks, "measured", {"sm_mhz": 2002.0, "sm_max_mhz": 2070.0})
+    assert p == 1887.4   # within 5 % of the maximum clock
+    p, note = bench.tensor_peak(peaks, "measured", {"sm_mhz": 1462.0, "sm_max_mhz": 2070.0})
+    assert abs(p - 1887.4 * 1462 / 2070) < 0.1 and "1462" in note
+    p, _ = bench.tensor_peak(peaks, "measured", {"sm_mhz": None, "sm_max_mhz": None})
+    assert p == 1887.4
+
+
+def test_forward_configs_bound_by_their_arithmetic_intensity():
+    from tiled_attention_07_gb300 import workloads as W
+
+    peaks = {"hbm_gbs": 6787.6, "bf16_tflops": 1887.4}
+    bounds = {cid: bench.forward_roofline(W.WORKLOADS[name], 0.1, peaks, 1887.4)["bound"]
+              for cid, name in bench.FORWARD_CONFIGS}
+    assert bounds == {"C1": "hbm", "C2": "tensor", "C3": "hbm", "C4": "tensor"}
+    w = W.WORKLOADS["bf16_b4_h20_n4096_d64_causal"]
+    r = bench.forward_roofline(w, 0.2, peaks, 1887.4)
+    assert abs(r["tflops"] - w.fwd_flops() / 0.2e-3 / 1e12) < 0.01
+    assert abs(r["frac"] - r["tflops"] / 1887.4) < 1e-4 and r["unit"] == "TFLOP/s"
