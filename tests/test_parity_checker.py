@@ -63,8 +63,9 @@ def test_correct_results_pass(setup):
     stats = {}
     check_grads(w.dtype, rounded, exact, naive, "rounded oracle", stats)
     check_grads(w.dtype, naive, exact, naive, "naive", stats)
-    # the rounded exact result sits well inside the bound
+    # the rounded exact result sits well inside both bounds
     assert max(stats[f"max_row_ratio_{n}"] for n in ("dq", "dk", "dv")) < 1.0, stats
+    assert max(stats[f"max_tile_ratio_{n}"] for n in ("dq", "dk", "dv")) < 1.0, stats
 
 
 def _rows_below_head_tolerance(dtype, a):
@@ -100,8 +101,8 @@ def _mutants(w, g):
     m["dk"][[5, 6]] = m["dk"][[6, 5]]
     out.append(("two adjacent dK rows swapped", m))
     m = {n: a.copy() for n, a in g.items()}
-    m["dq"] = _round(m["dq"] * 0.995, w.dtype)
-    out.append(("dQ 0.5 % low everywhere", m))
+    m["dq"] = _round(m["dq"] * 0.99, w.dtype)
+    out.append(("dQ 1 % low everywhere", m))
     return out
 
 
@@ -124,6 +125,19 @@ def test_small_rows_zeroed_pass_the_per_head_bound_alone():
     assert _per_head_bound_only(w.dtype, m, exact)
     with pytest.raises(AssertionError, match="dv row"):
         check_grads(w.dtype, m, exact, naive, name, {})
+
+
+def test_short_causal_rows_with_a_few_ulps_of_error_pass():
+    # A correct kernel's error on a row that sums a handful of terms can be
+    # several times the naive reference's (both are a few random roundings):
+    # three half-ulps of error on each early dQ row must still pass.
+    w, exact, naive, rounded = _setup(("bf16", 1024, 1024, 80, True, 1.0))
+    m = {n: a.copy() for n, a in rounded.items()}
+    rng = np.random.default_rng(0)
+    for i in range(1, 8):
+        row = exact["dq"][i]
+        m["dq"][i] = row + 3 * half_ulp(row, w.dtype) * rng.choice([-1.0, 1.0], size=row.shape)
+    check_grads(w.dtype, m, exact, naive, "early rows", {})
 
 
 def test_naive_reference_follows_the_definition():
