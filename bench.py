@@ -383,6 +383,11 @@ FORWARD_CONFIGS = (
 )
 
 
+#: The backward timed on both backward paths for the 'configs' key: the d = 64
+#: long causal shape (the fused path exists at d = 64 only).
+BACKWARD_CONFIG = ("C4_bwd", "bf16_b4_h20_n4096_d64_causal")
+
+
 def time_forward(fwd, stream, steps, warmup, flush):
     """Mean device time (ms) of `fwd()` over `steps` calls, each bracketed by
     CUDA events on `stream`; with `flush` (a buffer larger than L2) written
@@ -457,8 +462,37 @@ def run_configs(args, dev, peaks, peak_src):
                     "l2": "256 MB write between forwards" if in_bytes < (256 << 20) else "inputs larger than L2"}
         out[cid]["_ms"] = ms
         del x, o, lse
+    # the d = 64 backward of the long causal shape on both backward paths
+    w = W.WORKLOADS[BACKWARD_CONFIG[1]]
+    host = W.make_inputs(w, device="cpu", with_grad_output=True)
+    x = {k: t.to(dev) for k, t in host.items()}
+    o = torch.empty_like(x["q"])
+    lse = torch.empty(fa.lse_shape(x["q"]), dtype=torch.float32, device=dev)
+    fa.fa_fwd(x["q"], x["k"], x["v"], o, lse, w.sm_scale, w.causal, stream)
+    grads = {n: torch.empty_like(x[src]) for n, src in (("dq", "q"), ("dk", "k"), ("dv", "v"))}
+    B, H, Nq, d = fa._dims(x["q"])
+    bwd = {}
+    for path_name, path in (("two_pass", fa.FA_BWD_PATH_TWO_PASS), ("fused", fa.FA_BWD_PATH_FUSED)):
+        ws = torch.empty(fa.fa_bwd_workspace_bytes_path(B, H, Nq, Nq, d, path), dtype=torch.uint8, device=dev)
+
+        def run(path=path, ws=ws):
+            fa.fa_bwd_ex(path, 0, x["q"], x["k"], x["v"], o, x["do"], lse, grads["dq"], grads["dk"], grads["dv"],
+                         w.sm_scale, w.causal, ws, stream)
+
+        ms = time_forward(run, stream, args.config_steps, 10, flush)
+        rc, detail = fa.fa_last_device_error(stream)
+        if rc != fa.FA_OK:
+            raise RuntimeError(f"device error in the {path_name} backward: {detail:#x}")
+        bwd[path_name] = {"ms": round(ms, 5), "launches": args.config_steps * 3, "_ms": ms}
+        del ws
+    del x, o, lse, grads
     clk = clocks.stop()
     tpeak, tnote = tensor_peak(peaks, peak_src, clk)
+    for entry in bwd.values():
+        tf = w.bwd_flops() / (entry.pop("_ms") / 1e3) / 1e12
+        entry.update({"tflops_credited": round(tf, 2), "frac": round(tf / tpeak, 4), "peak": tpeak})
+    out[BACKWARD_CONFIG[0]] = {"workload": w.name, "steps": args.config_steps, "l2": "256 MB write between calls",
+                               "credit": "10*B*H*N^2*d/2 (five products)", "paths": bwd}
     for cid, name in FORWARD_CONFIGS:
         w = W.WORKLOADS[name]
         ms = out[cid].pop("_ms")

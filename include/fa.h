@@ -191,9 +191,10 @@ FA_API fa_status fa_fwd_fp8v(const void* q, const void* k, const void* vt, void*
 /*
  * fa_bwd_workspace_bytes -- size of the scratch buffer fa_bwd needs: the
  * per-row D = rowsum(O o dO) and the log2-domain LSE, float32, padded to
- * whole 128-row query tiles: 2 * 4 * B*H*ceil(Nq/128)*128 bytes.  ("[CS336]",
- * "FlashAttention V2 / Backward Pass": D is computed once, before the two
- * passes, and kept in global memory.)
+ * whole 128-row query tiles: 2 * 4 * B*H*ceil(Nq/128)*128 bytes, plus a
+ * float32 dQ accumulator row per query where the fused path is the faster
+ * one (see fa_bwd_path below).  ("[CS336]", "FlashAttention V2 / Backward
+ * Pass": D is computed once, before the passes, and kept in global memory.)
  */
 FA_API size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int Nk, int d);
 
@@ -206,6 +207,7 @@ FA_API size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int Nk, int d);
  *   dq [B, H, Nq, d], dk, dv [B, H, Nk, d]: out, input dtype
  *   workspace: device buffer of at least fa_bwd_workspace_bytes() bytes,
  *   16-byte aligned, owned by the caller; its contents on entry are ignored.
+ *   (A workspace of only the two-pass size selects the two-pass path.)
  * Returns FA_ERR_WORKSPACE if the workspace is NULL or too small.
  */
 FA_API fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
@@ -245,6 +247,52 @@ FA_API fa_status fa_bwd_phase(int phase, const void* q, const void* k, const voi
                        void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Backward paths.
+ *   FA_BWD_PATH_TWO_PASS: the scheme of "[CS336]", "FlashAttention V2 /
+ *     Backward Pass": dK and dV accumulate along query tiles and dQ along key
+ *     tiles, so one pass over query tiles forms dK, dV and one over key tiles
+ *     forms dQ, each recomputing P (seven products per tile pair).  Every
+ *     output is bitwise reproducible.  Any d.
+ *   FA_BWD_PATH_FUSED (d = 64 only): one pass over key tiles.  Besides dK and
+ *     dV it forms each query tile's share of dQ and adds it into a float32
+ *     accumulator in the workspace (reductions performed in L2), then a
+ *     short launch converts the accumulator to dQ.  That is the five products
+ *     of the recompute equations.  The order of the float32 additions into dQ
+ *     varies from run to run, so dQ (not dK, dV) may differ in the last bits
+ *     between runs.
+ *   FA_BWD_PATH_AUTO: the path measured faster at this head dim, when the
+ *     workspace holds it; otherwise the two-pass path.  This is what fa_bwd,
+ *     fa_bwd_strided and fa_bwd_phase do, and fa_bwd_workspace_bytes gives
+ *     the size of the path AUTO prefers.
+ */
+typedef enum { FA_BWD_PATH_AUTO = 0, FA_BWD_PATH_TWO_PASS = 1, FA_BWD_PATH_FUSED = 2 } fa_bwd_path;
+
+/*
+ * fa_bwd_workspace_bytes_path -- workspace bytes of one path: two-pass
+ * 2 * 4 * B*H*ceil(Nq/128)*128 (D and the log2-domain LSE); fused
+ * (2 + d) * 4 * B*H*ceil(Nq/128)*128 (the same, then a float32 dQ row per
+ * query); AUTO as fa_bwd_workspace_bytes.  0 for the fused path at a head dim
+ * it does not support, and for empty problems.
+ */
+FA_API size_t fa_bwd_workspace_bytes_path(int B, int H, int Nq, int Nk, int d, fa_bwd_path path);
+
+/*
+ * fa_bwd_ex -- the backward on a chosen path, whole (phase 0) or one launch
+ * at a time (phases 1-3 as fa_bwd_phase: on the fused path 1 also zeroes the
+ * dQ accumulator, 2 forms dK, dV and adds dQ's partial sums into the
+ * accumulator, 3 writes dQ from it).  layout == NULL means contiguous
+ * [B, H, seq, d].  The workspace must hold fa_bwd_workspace_bytes_path() of
+ * the path taken, else FA_ERR_WORKSPACE.  FA_BWD_PATH_FUSED at a head dim
+ * other than 64 gives FA_ERR_UNSUPPORTED; an unknown path or phase
+ * FA_ERR_INVALID_ARG.  Other arguments and errors as fa_bwd_strided.
+ */
+FA_API fa_status fa_bwd_ex(fa_bwd_path path, int phase, const void* q, const void* k, const void* v,
+                    const void* o, const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                    int B, int H, int Nq, int Nk, int d, float sm_scale, int causal,
+                    fa_dtype dtype, const fa_layout* layout,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * fa_bwd_noalloc -- fa_bwd for callers that cannot allocate device memory.
  * The pages have no counterpart to it.  It serves callers that are handed
  * only their input and output buffers and may not allocate on their own, for
@@ -254,6 +302,7 @@ FA_API fa_status fa_bwd_phase(int phase, const void* q, const void* k, const voi
  * FA_NOALLOC_SCRATCH_BYTES that the library keeps in every GPU that loads
  * it, until the process exits.
  *   Arguments: as fa_bwd (contiguous [B, H, seq, d]), without the workspace.
+ *   Path: always the two-pass backward (its scratch needs 8 bytes per row).
  *   Limit: B*H*ceil(Nq/128)*128 <= FA_NOALLOC_SCRATCH_BYTES / 8 query rows
  *   (2,097,152; e.g. B=4, H=32, Nq=16384).  Larger problems return
  *   FA_ERR_WORKSPACE before anything is launched.

@@ -210,20 +210,49 @@ fa_status fwd_fp8v_impl(const void* q, const void* k, const void* vt, void* o, f
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
+// Workspace of the two-pass backward: D and log2-LSE, float32, per padded row.
 size_t ws_bytes(int B, int H, int Nq) {
   if (B <= 0 || H <= 0 || Nq <= 0) return 0;
   const size_t rows = mul_sat(static_cast<size_t>(B) * static_cast<size_t>(H), static_cast<size_t>(nq_pad(Nq)));
   return mul_sat(2 * sizeof(float), rows);
 }
 
+// Workspace of the fused backward: D, log2-LSE and a float32 dQ row each.
+size_t ws_bytes_fused(int B, int H, int Nq, int d) {
+  if (B <= 0 || H <= 0 || Nq <= 0 || d <= 0) return 0;
+  const size_t rows = mul_sat(static_cast<size_t>(B) * static_cast<size_t>(H), static_cast<size_t>(nq_pad(Nq)));
+  return mul_sat(sizeof(float) * (2 + static_cast<size_t>(d)), rows);
+}
+
+// The path FA_BWD_PATH_AUTO prefers at head dim d (the one measured faster
+// on the backward workloads with that head dim).
+bool fused_preferred(int d) { return false && bwd_fused_supported(d); }
+
+size_t ws_bytes_path(int B, int H, int Nq, int d, fa_bwd_path path) {
+  switch (path) {
+    case FA_BWD_PATH_TWO_PASS: return ws_bytes(B, H, Nq);
+    case FA_BWD_PATH_FUSED: return bwd_fused_supported(d) ? ws_bytes_fused(B, H, Nq, d) : 0;
+    case FA_BWD_PATH_AUTO: return fused_preferred(d) ? ws_bytes_fused(B, H, Nq, d) : ws_bytes(B, H, Nq);
+  }
+  return 0;
+}
+
 fa_status bwd_impl(const Tensor4& q, const Tensor4& k, const Tensor4& v, const Tensor4& o, const Tensor4& dout,
                    const float* lse, const Tensor4& dq, const Tensor4& dk, const Tensor4& dv, int B, int H, int Nq,
                    int Nk, int d, float sm_scale, int causal, fa_dtype dtype, void* workspace,
-                   size_t workspace_bytes, int phase, void* stream) {
+                   size_t workspace_bytes, int phase, void* stream, fa_bwd_path path = FA_BWD_PATH_AUTO) {
   if (phase < 0 || phase > 3) return FA_ERR_INVALID_ARG;
+  if (path != FA_BWD_PATH_AUTO && path != FA_BWD_PATH_TWO_PASS && path != FA_BWD_PATH_FUSED)
+    return FA_ERR_INVALID_ARG;
   fa_status st = check_common(B, H, Nq, Nk, d, sm_scale, causal, dtype);
   if (st != FA_OK) return st;
+  if (path == FA_BWD_PATH_FUSED && !bwd_fused_supported(d)) return FA_ERR_UNSUPPORTED;
   if (B == 0 || H == 0) return FA_OK;
+  // AUTO takes the preferred path when the workspace holds it, else the
+  // two-pass path.
+  const bool fused = path == FA_BWD_PATH_FUSED ||
+                     (path == FA_BWD_PATH_AUTO && fused_preferred(d) &&
+                      workspace_bytes >= ws_bytes_fused(B, H, Nq, d));
   // With no queries only dK = dV = 0 is written; the query-side tensors, lse
   // and the workspace are not touched.
   if (!valid_tensor(k) || !valid_tensor(v) || !valid_tensor(dk) || !valid_tensor(dv)) return FA_ERR_INVALID_ARG;
@@ -231,8 +260,8 @@ fa_status bwd_impl(const Tensor4& q, const Tensor4& k, const Tensor4& v, const T
     if (!valid_tensor(q) || !valid_tensor(o) || !valid_tensor(dout) || !valid_tensor(dq))
       return FA_ERR_INVALID_ARG;
     if (lse == nullptr || !aligned16(lse)) return FA_ERR_INVALID_ARG;
-    if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < ws_bytes(B, H, Nq))
-      return FA_ERR_WORKSPACE;
+    const size_t need = fused ? ws_bytes_fused(B, H, Nq, d) : ws_bytes(B, H, Nq);
+    if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < need) return FA_ERR_WORKSPACE;
   }
   if (get_encode() == nullptr) return FA_ERR_CUDA;
   cudaError_t e;
@@ -258,6 +287,7 @@ fa_status bwd_impl(const Tensor4& q, const Tensor4& k, const Tensor4& v, const T
   a.causal = causal;
   a.bf16 = dtype == FA_BF16;
   a.err = err;
+  a.fused = fused;
   e = launch_bwd(a, phase, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -359,8 +389,12 @@ fa_status fa_fwd_split(const void* q, const void* k, const void* v, void* o, flo
 
 size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int Nk, int d) {
   (void)Nk;
-  (void)d;
-  return fa::ws_bytes(B, H, Nq);
+  return fa::ws_bytes_path(B, H, Nq, d, FA_BWD_PATH_AUTO);
+}
+
+size_t fa_bwd_workspace_bytes_path(int B, int H, int Nq, int Nk, int d, fa_bwd_path path) {
+  (void)Nk;
+  return fa::ws_bytes_path(B, H, Nq, d, path);
 }
 
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
@@ -397,6 +431,22 @@ fa_status fa_bwd_phase(int phase, const void* q, const void* k, const void* v, c
                       fa::strided(o, layout->o), fa::strided(dout, layout->dout), lse,
                       fa::strided(dq, layout->dq), fa::strided(dk, layout->dk), fa::strided(dv, layout->dv), B, H,
                       Nq, Nk, d, sm_scale, causal, dtype, workspace, workspace_bytes, phase, stream);
+}
+
+fa_status fa_bwd_ex(fa_bwd_path path, int phase, const void* q, const void* k, const void* v, const void* o,
+                    const void* dout, const float* lse, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk,
+                    int d, float sm_scale, int causal, fa_dtype dtype, const fa_layout* layout, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  if (phase < 0 || phase > 3) return FA_ERR_INVALID_ARG;
+  if (layout == nullptr)
+    return fa::bwd_impl(fa::contiguous(q, H, Nq, d), fa::contiguous(k, H, Nk, d), fa::contiguous(v, H, Nk, d),
+                        fa::contiguous(o, H, Nq, d), fa::contiguous(dout, H, Nq, d), lse,
+                        fa::contiguous(dq, H, Nq, d), fa::contiguous(dk, H, Nk, d), fa::contiguous(dv, H, Nk, d),
+                        B, H, Nq, Nk, d, sm_scale, causal, dtype, workspace, workspace_bytes, phase, stream, path);
+  return fa::bwd_impl(fa::strided(q, layout->q), fa::strided(k, layout->k), fa::strided(v, layout->v),
+                      fa::strided(o, layout->o), fa::strided(dout, layout->dout), lse,
+                      fa::strided(dq, layout->dq), fa::strided(dk, layout->dk), fa::strided(dv, layout->dv), B, H,
+                      Nq, Nk, d, sm_scale, causal, dtype, workspace, workspace_bytes, phase, stream, path);
 }
 
 const char* fa_status_string(fa_status s) {

@@ -14,6 +14,17 @@
 //                    sixteen elementwise warps, dV += P^T dO_i, dK += dS^T Q_i
 //   dq_kernel        one CTA per 128-query tile, loop over key tiles:
 //                    S = Q K_j^T, dP = dO V_j^T, dS, dQ += dS K_j
+// At d = 64 the library also has a single-pass form (the "fused" backward):
+//   dkdv_kernel<.., FUSED>  as dkdv_kernel, and besides dK and dV it forms
+//                    each query tile's share of dQ, dQ_i += dS_i K (dS_i
+//                    written to shared memory by the elementwise warps, the
+//                    product into TMEM), and adds it into a float32 dQ
+//                    accumulator in the workspace with vector reductions;
+//   dq_convert_kernel  dQ = sm_scale * accumulator, in the input type.
+// It computes the five products of the recompute equations instead of the
+// two passes' seven, at the cost of the reductions into L2; the order of the
+// float32 additions into dQ then varies from run to run (dQ is not bitwise
+// deterministic, dK and dV are).
 // P is exp2(c S - L log2 e) with c = sm_scale log2(e) ("Fused Attention 2":
 // exp2 with the scale folded by log2 e).  P^T and dS^T (dS) are rounded to the
 // input type and written back into the TMEM columns they were computed from,
@@ -64,6 +75,7 @@ struct PreParams {
   const float* lse;
   float* wsD;
   float* wsL;
+  float* dqacc;   // fused backward: float32 dQ accumulator rows, zeroed here (else null)
   int B, H, Nq, Nqp, d;
 };
 
@@ -104,6 +116,10 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreParams p) {
     p.wsD[row] = valid ? acc : 0.f;
     p.wsL[row] = valid ? -p.lse[static_cast<long long>(bh) * p.Nq + q] * kLog2e : -CUDART_INF_F;
   }
+  if (active && p.dqacc != nullptr) {
+    float4* z = reinterpret_cast<float4*>(p.dqacc + row * p.d);
+    for (int c = sub; c < p.d / 4; c += 8) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
 }
 
 // zero dK and dV when there are no queries
@@ -133,6 +149,11 @@ struct BwdCfg {
   static constexpr int KV_NSTAGE = D == 64 ? 5 : (D == 80 ? 3 : 2);
   static constexpr int KV_STAGE = 2 * TILE + 2 * 512;
   static constexpr int KV_SMEM = 1024 + 2 * TILE + KV_NSTAGE * KV_STAGE + 512;
+  // fused dK/dV/dQ (d = 64): one ring stage less than dK/dV alone, to make
+  // room for the 128 x 128 16-bit dS tile
+  static constexpr int KVQ_NSTAGE = KV_NSTAGE - 1;
+  static constexpr int DS_TILE = 128 * 128 * 2;
+  static constexpr int KVQ_SMEM = 1024 + 2 * TILE + KVQ_NSTAGE * KV_STAGE + DS_TILE + 512;
   // dQ: Q, dO resident; ring of (K_j, V_j)
   static constexpr int Q_NSTAGE = D == 64 ? 5 : (D == 80 ? 3 : 2);
   static constexpr int Q_STAGE = 2 * TILE;
@@ -174,6 +195,21 @@ __device__ __forceinline__ void mma_tn(uint32_t d_tmem, uint32_t a_tmem, uint32_
   }
 }
 
+// D(128 x D) = A(128 x 128) * B(128 x D), both MN-major tiles in shared
+// memory: A a 128-column tile (two 64-column chunks; M along its columns, K
+// along its rows), B a tile of D columns (N along its columns, K along its
+// rows).  Used for dQ_i = dS_i K with dS_i stored keys x queries.
+template <int D>
+__device__ __forceinline__ void mma_mn_mn(uint32_t d_tmem, uint32_t a_addr, uint32_t b_addr, uint32_t idesc) {
+  using GA = TileGeo<128>;
+  using G = TileGeo<D>;
+  const uint64_t ad0 = make_sdesc(a_addr, GA::CHB, GA::SBO, GA::LAYOUT);
+  const uint64_t bd0 = make_sdesc(b_addr, G::CHB, G::SBO, G::LAYOUT);
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks)
+    if (elect_one()) umma_ss(d_tmem, desc_add(ad0, ks * 16 * GA::ROWB), desc_add(bd0, ks * 16 * G::ROWB), idesc, ks > 0);
+}
+
 // Folding L and D into the GEMMs (bf16, d = 80): the tiles of d = 80 carry
 // 16 zero-filled padding columns [80, 96).  With 1 in columns 80 and 81 of K
 // and V, and a two-term bf16 split of -L log2(e) / c and of -D in columns 80
@@ -209,6 +245,7 @@ struct MainParams {
   int64_t o0_sb, o0_sh, o0_ss;
   void* out1;         // dkdv: dK
   int64_t o1_sb, o1_sh, o1_ss;
+  float* dqacc;       // fused dkdv: float32 dQ accumulator [B*H][Nqp][D]
   int* err;
 };
 
@@ -237,13 +274,19 @@ __device__ __forceinline__ void store16(uint8_t* dst, const uint32_t (&v)[16], f
 // tile i; with d = 128 there is no room and P^T overwrites S^T.  Elementwise warps:
 // warpgroup g = warp / 4 owns query columns [32 g, 32 g + 32); warp % 4
 // selects the 32 key rows.
-template <int D, bool BF16>
+// FUSED (d = 64): also dQ.  The elementwise warps write dS_i = (dS^T_i)^T
+// into a shared-memory tile (keys x queries) besides the 16-bit dS^T in
+// TMEM; issuer B computes dQ_i = dS_i K into the last 64 TMEM columns (lanes
+// = queries), and the elementwise warps add that into the float32
+// accumulator during the next step (red.global.add), then release the
+// columns.  The dS tile is rewritten only after dQ_i has completed.
+template <int D, bool BF16, bool FUSED = false>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                 const MainParams p) {
   using C = BwdCfg<D>;
-  constexpr int NS = C::KV_NSTAGE;
+  constexpr int NS = FUSED ? C::KVQ_NSTAGE : C::KV_NSTAGE;
   // kSepP: P^T has a 64-column region of its own (see above).
   constexpr bool kSepP = 256 + 2 * D + 64 <= 512;
   // kFold: L and D folded into the padded GEMMs (see fold_slot).
@@ -252,12 +295,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   constexpr uint32_t kColDV = 256;
   constexpr uint32_t kColDK = kSepP ? 256 + D : 384;
   constexpr uint32_t kColP = kSepP ? 256 + 2 * D : 0;
+  constexpr uint32_t kColDQ = kColP + 64;   // FUSED: dQ_i, D columns
+  static_assert(!FUSED || (kSepP && !kFold && kColDQ + D <= 512), "the fused layout fits d = 64 only");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = smem;
   uint8_t* sV = smem + C::TILE;
   uint8_t* sStage = smem + 2 * C::TILE;   // per stage: Q, dO, L[128], D[128]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sStage + NS * C::KV_STAGE);
+  uint8_t* sDS = sStage + NS * C::KV_STAGE;   // FUSED: dS_i, 128 keys x 128 queries, two 64-query chunks
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sDS + (FUSED ? C::DS_TILE : 0));
   uint64_t* bar_kv = bars;            // K, V loaded
   uint64_t* bar_full = bars + 1;      // [NS]
   uint64_t* bar_empty = bar_full + NS;
@@ -270,7 +316,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   uint64_t* bar_sfree = bar_drain + 1;  // S^T read into registers (separate-P^T layout)
   uint64_t* bar_dvd = bar_sfree + 1;    // dV_i complete: P^T_i consumed
   uint64_t* bar_ext = bar_dvd + 1;      // folded columns of K, V, Q_0, dO_0 written (kFold)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_ext + 1);
+  uint64_t* bar_dq = bar_ext + 1;       // FUSED: dQ_i complete
+  uint64_t* bar_dqfree = bar_dq + 1;    // FUSED: dQ_i read out of TMEM (one arrival per elementwise warp)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_dqfree + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -301,6 +349,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     mbar_init(bar_sfree, C::EW_WARPS);
     mbar_init(bar_dvd, 1);
     mbar_init(bar_ext, C::EW_WARPS);
+    mbar_init(bar_dq, 1);
+    mbar_init(bar_dqfree, C::EW_WARPS);
     fence_mbar_init();
   }
   if (warp == C::MMA_WARP) {
@@ -402,6 +452,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           __syncwarp();
           tc_fence_after();
           mma_tn<D>(tmem + kColDK, tmem + 128, sq, idesc_tn, it > 0);  // dK += dS^T_i Q_i
+          if constexpr (FUSED) {
+            constexpr uint32_t idesc_dq = make_idesc_f16(BF16, kT, D, true, true);
+            if (it > 0) {
+              mbar_wait(bar_dqfree, (it - 1) & 1, p.err, 52);   // dQ_{i-1} read out of TMEM
+              __syncwarp();
+              tc_fence_after();
+            }
+            mma_mn_mn<D>(tmem + kColDQ, smem_u32(sDS), sk, idesc_dq);   // dQ_i = dS_i K
+            if (elect_one()) umma_commit(bar_dq);
+          }
         }
         if (elect_one()) umma_commit(&bar_empty[s]);
       }
@@ -424,6 +484,24 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const uint64_t cs2 = f2pack(p.scale_log2, p.scale_log2);
     const int kr = quad * 32 + lane;   // this thread's row of the K/V tile and of the stage rows it folds
 
+    // FUSED: add dQ_j (TMEM lanes = the 128 queries of query tile j) into the
+    // accumulator.  Warp (g, quad) takes lanes [32 quad, 32 quad + 32) and
+    // columns [16 g, 16 g + 16): four 16-byte reductions per thread.
+    auto reduce_dq = [&](int j) {
+      mbar_wait(bar_dq, j & 1, p.err, 53);
+      tc_fence_after();
+      uint32_t v[16];
+      tmem_ld16(tmem + lane_off + kColDQ + g * 16, v);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_dqfree);
+      float* dst = p.dqacc + (static_cast<size_t>(bh) * p.Nqp + (i_first + j) * kT + quad * 32 + lane) * D + g * 16;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        red_add_f32x4(dst + 4 * c, __uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
+                      __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]));
+    };
     // Folded columns of stage s: Q rows by warpgroup 2 (-L log2 e / c), dO
     // rows by warpgroup 3 (-D); L and D come with the stage.
     auto fold_stage = [&](int s) {
@@ -498,6 +576,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         for (int e = 0; e < 32; ++e)
           if (q0 + e < krow) pt[e] = 0.f;
       }
+      if (FUSED && krow >= p.Nk) {
+        // keys past Nk (zero-filled K, V rows) must add nothing to dQ
+#pragma unroll
+        for (int e = 0; e < 32; ++e) pt[e] = 0.f;
+      }
       {
         uint32_t pk[16];
 #pragma unroll
@@ -512,6 +595,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_pt);
+
+      if (FUSED && it > 0) reduce_dq(it - 1);
 
       mbar_wait(bar_dp, it & 1, p.err, 29);
       tc_fence_after();
@@ -542,12 +627,25 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
           pk[e / 2 + 1] = pack2<BF16>(a2, a3);
         }
         tmem_st16(tdP, pk);
+        if constexpr (FUSED) {
+          // dS_i row kr (this thread's key), queries [32 g, 32 g + 32): 64
+          // bytes of 64-query chunk g / 2, 16-byte granules 4 (g % 2) .. + 3,
+          // 128-byte swizzle.  dQ_{i-1}, the last reader of the tile, has
+          // completed (reduce_dq waited for it).
+          uint8_t* row = sDS + (g >> 1) * TileGeo<128>::CHB + kr * 128;
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<uint4*>(row + ((((g & 1) * 4 + c) ^ (kr & 7)) << 4)) =
+                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          fence_proxy_async_smem();
+        }
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ds);
     }
+    if (FUSED && n_it > 0) reduce_dq(n_it - 1);
 
     // epilogue: warpgroups 0-1 write dV, 2-3 write dK * sm_scale (16-column
     // chunks alternate between the two warpgroups of each)
@@ -851,6 +949,38 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   }
 }
 
+// dQ = sm_scale * accumulator, in the input type: one thread per 8 columns of
+// a row (two 16-byte loads, one 16-byte store); padded rows are not stored.
+struct ConvertParams {
+  const float* acc;   // [B*H][Nqp][D]
+  void* dq;
+  int64_t sb, sh, ss;
+  int H, Nq, Nqp;
+  long long rows;     // B*H*Nq
+  float scale;
+};
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) dq_convert_kernel(const ConvertParams p) {
+  constexpr int kGroups = D / 8;
+  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= p.rows * kGroups) return;
+  const int c = static_cast<int>(t % kGroups);
+  const long long r = t / kGroups;
+  const int q = static_cast<int>(r % p.Nq);
+  const int bh = static_cast<int>(r / p.Nq);
+  const float4* src = reinterpret_cast<const float4*>(p.acc + (static_cast<size_t>(bh) * p.Nqp + q) * D + 8 * c);
+  const float4 a = src[0], b = src[1];
+  const float s = p.scale;
+  uint4 w;
+  w.x = pack2<BF16>(a.x * s, a.y * s);
+  w.y = pack2<BF16>(a.z * s, a.w * s);
+  w.z = pack2<BF16>(b.x * s, b.y * s);
+  w.w = pack2<BF16>(b.z * s, b.w * s);
+  uint8_t* dst = const_cast<uint8_t*>(row_ptr(p.dq, p.sb, p.sh, p.ss, bh / p.H, bh % p.H, q));
+  reinterpret_cast<uint4*>(dst)[c] = w;
+}
+
 template <int D, bool BF16>
 cudaError_t launch_bwd_t(const BwdArgs& a, int phase, cudaStream_t stream) {
   using C = BwdCfg<D>;
@@ -882,6 +1012,8 @@ cudaError_t launch_bwd_t(const BwdArgs& a, int phase, cudaStream_t stream) {
   pp.lse = a.lse;
   pp.wsD = wsD;
   pp.wsL = wsL;
+  float* dqacc = a.fused ? a.ws + 2 * static_cast<size_t>(BH) * Nqp : nullptr;
+  pp.dqacc = dqacc;
   pp.B = a.B;
   pp.H = a.H;
   pp.Nq = a.Nq;
@@ -912,6 +1044,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, int phase, cudaStream_t stream) {
   mp.sm_scale = a.sm_scale;
   mp.wsD = wsD;
   mp.wsL = wsL;
+  mp.dqacc = dqacc;
   mp.err = a.err;
 
   // dK, dV
@@ -923,6 +1056,38 @@ cudaError_t launch_bwd_t(const BwdArgs& a, int phase, cudaStream_t stream) {
   mp.o1_sb = a.dk.sb;
   mp.o1_sh = a.dk.sh;
   mp.o1_ss = a.dk.ss;
+  if (a.fused) {
+    if constexpr (D == 64) {
+      if (phase == 0 || phase == 2) {
+        auto kern = dkdv_kernel<D, BF16, true>;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::KVQ_SMEM);
+        if (e != cudaSuccess) return e;
+        const long long blocks = static_cast<long long>((a.Nk + kT - 1) / kT) * BH;
+        kern<<<static_cast<unsigned>(blocks), C::THREADS, C::KVQ_SMEM, stream>>>(tq, tk, tv, tdo, mp);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+      }
+      if (phase == 0 || phase == 3) {
+        ConvertParams cp;
+        cp.acc = dqacc;
+        cp.dq = const_cast<void*>(a.dq.ptr);
+        cp.sb = a.dq.sb;
+        cp.sh = a.dq.sh;
+        cp.ss = a.dq.ss;
+        cp.H = a.H;
+        cp.Nq = a.Nq;
+        cp.Nqp = Nqp;
+        cp.rows = static_cast<long long>(BH) * a.Nq;
+        cp.scale = a.sm_scale;
+        const long long threads = cp.rows * (D / 8);
+        dq_convert_kernel<D, BF16><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(cp);
+        e = cudaGetLastError();
+      }
+      return e;
+    } else {
+      return cudaErrorInvalidValue;
+    }
+  }
   if (phase == 0 || phase == 2) {
     auto kern = dkdv_kernel<D, BF16>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::KV_SMEM);

@@ -36,12 +36,14 @@ struct FwdArgs {
 struct BwdArgs {
   Tensor4 q, k, v, o, dout, dq, dk, dv;
   const float* lse;  // [B, H, Nq] fp32
-  float* ws;         // workspace: D and log2-domain LSE, [B*H][Nq_pad] each
+  float* ws;         // workspace: D and log2-domain LSE, [B*H][Nq_pad] each;
+                     // fused: then the float32 dQ accumulator [B*H][Nq_pad][d]
   int B, H, Nq, Nk, d;
   float sm_scale;
   int causal;
   bool bf16;
   int* err;
+  bool fused = false;   // one pass over key tiles for dK, dV and dQ (d = 64)
 };
 
 // Rows per query / key tile of every kernel (one TMEM lane per row).
@@ -94,7 +96,11 @@ bool make_vt_map(CUtensorMap* map, const void* vt, int64_t ld, int Nk, int d, in
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 // phase: 0 = all three launches; 1 = D / log2-LSE preprocess; 2 = dK, dV;
-// 3 = dQ (phases 2 and 3 read what phase 1 wrote to the workspace).
+// 3 = dQ (phases 2 and 3 read what phase 1 wrote to the workspace).  With
+// a.fused: 1 also zeroes the dQ accumulator, 2 = dK, dV and dQ's partial
+// sums (added into the accumulator), 3 = dQ from the accumulator.
 cudaError_t launch_bwd(const BwdArgs& a, int phase, cudaStream_t stream);
+// Head dims the fused backward is built for.
+inline bool bwd_fused_supported(int d) { return d == 64; }
 
 }  // namespace fa

@@ -53,7 +53,9 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
                                     const float* lse, void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk,
                                     int d, float sm_scale, int causal, fa_dtype dtype, void* stream) {
   // Reject problems whose scratch does not fit before touching the device.
-  if (fa_bwd_workspace_bytes(B, H, Nq, Nk, d) > kScratchBytes) return FA_ERR_WORKSPACE;
+  // The scratch holds the two-pass backward's D and log2-LSE only, so this
+  // entry point always takes that path.
+  if (fa_bwd_workspace_bytes_path(B, H, Nq, Nk, d, FA_BWD_PATH_TWO_PASS) > kScratchBytes) return FA_ERR_WORKSPACE;
   void* scratch = nullptr;
   if (B > 0 && H > 0 && Nq > 0) {
     const fa_status st = scratch_for_current_device(&scratch);
@@ -62,6 +64,6 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
   // The preprocess launch overwrites every scratch entry the two later
   // launches read (padding rows included), so stale contents from an earlier
   // call need no clearing.
-  return fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, Nq, Nk, d, sm_scale, causal, dtype, scratch,
-                kScratchBytes, stream);
+  return fa_bwd_ex(FA_BWD_PATH_TWO_PASS, 0, q, k, v, o, dout, lse, dq, dk, dv, B, H, Nq, Nk, d, sm_scale, causal,
+                   dtype, nullptr, scratch, kScratchBytes, stream);
 }

@@ -358,6 +358,16 @@ __device__ __forceinline__ void tmem_reg_tie(uint32_t (&r)[32]) {
 #undef FA_R16
 
 // ---------------------------------------------------------------------------
+// Reductions into global memory
+// ---------------------------------------------------------------------------
+// [addr, addr + 16) += (a, b, c, d), float32, performed in L2 (no return
+// value); addr 16-byte aligned.
+__device__ __forceinline__ void red_add_f32x4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+// ---------------------------------------------------------------------------
 // Per-warpgroup register budgets (all four warps of a warpgroup execute it)
 // ---------------------------------------------------------------------------
 template <uint32_t N>

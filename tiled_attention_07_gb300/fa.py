@@ -46,6 +46,10 @@ FA_BWD_PREPROCESS = 1
 FA_BWD_DKDV = 2
 FA_BWD_DQ = 3
 
+FA_BWD_PATH_AUTO = 0
+FA_BWD_PATH_TWO_PASS = 1
+FA_BWD_PATH_FUSED = 2
+
 EXPORTED_SYMBOLS = (
     "fa_fwd",
     "fa_fwd_strided",
@@ -57,6 +61,8 @@ EXPORTED_SYMBOLS = (
     "fa_bwd",
     "fa_bwd_strided",
     "fa_bwd_phase",
+    "fa_bwd_workspace_bytes_path",
+    "fa_bwd_ex",
     "fa_bwd_noalloc",
     "fa_softmax_rows",
     "fa_status_string",
@@ -120,6 +126,11 @@ def lib() -> ctypes.CDLL:
         L.fa_bwd_phase.argtypes = [i, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i,
                                    ctypes.POINTER(Layout), vp, ctypes.c_size_t, vp]
         L.fa_bwd_phase.restype = i
+        L.fa_bwd_workspace_bytes_path.argtypes = [i, i, i, i, i, i]
+        L.fa_bwd_workspace_bytes_path.restype = ctypes.c_size_t
+        L.fa_bwd_ex.argtypes = [i, i, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i,
+                                ctypes.POINTER(Layout), vp, ctypes.c_size_t, vp]
+        L.fa_bwd_ex.restype = i
         L.fa_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
         L.fa_bwd_noalloc.restype = i
         L.fa_softmax_rows.argtypes = [vp, vp, vp, i, i, ctypes.c_int64, ctypes.c_int64, i, vp]
@@ -378,6 +389,39 @@ def fa_bwd_phase(phase: int, q, k, v, o, do, lse, dq, dk, dv, sm_scale: float, c
                                 workspace.numel() * workspace.element_size(), _stream(stream, q.device))
     if rc != FA_OK:
         raise FaError(rc, f"fa_bwd_phase({phase})")
+
+
+def fa_bwd_workspace_bytes_path(B: int, H: int, Nq: int, Nk: int, d: int, path: int) -> int:
+    return int(lib().fa_bwd_workspace_bytes_path(B, H, Nq, Nk, d, int(path)))
+
+
+def fa_bwd_ex(path: int, phase: int, q, k, v, o, do, lse, dq, dk, dv, sm_scale: float, causal: bool,
+              workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """The backward on a chosen path (FA_BWD_PATH_*), whole (phase 0) or one
+    launch at a time; ``workspace`` defaults to a torch buffer of the path's
+    size (fa_bwd_workspace_bytes_path)."""
+    dt = _dtype_code(q)
+    _check_attention(q, k, v, o, lse, q_like={"do": do, "dq": dq}, k_like={"dk": dk, "dv": dv})
+    B, H, Nq, d = _dims(q)
+    _, _, Nk, _ = _dims(k)
+    if workspace is None:
+        need = fa_bwd_workspace_bytes_path(B, H, Nq, Nk, d, path)
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check_cuda(workspace)
+    _check_same_device(q, workspace)
+    ts = (q, k, v, o, do, dq, dk, dv)
+    lay = None
+    if not all(_is_bhsd_contiguous(t) for t in ts):
+        lay = Layout()
+        lay.q, lay.k, lay.v, lay.o = _strides(q), _strides(k), _strides(v), _strides(o)
+        lay.dout, lay.dq, lay.dk, lay.dv = _strides(do), _strides(dq), _strides(dk), _strides(dv)
+    with torch.cuda.device(q.device):
+        rc = lib().fa_bwd_ex(int(path), int(phase), *[_ptr(t) for t in (q, k, v, o, do, lse, dq, dk, dv)], B, H,
+                             Nq, Nk, d, float(sm_scale), int(bool(causal)), dt,
+                             None if lay is None else ctypes.byref(lay), _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), _stream(stream, q.device))
+    if rc != FA_OK:
+        raise FaError(rc, f"fa_bwd_ex(path {path}, phase {phase})")
 
 
 NOALLOC_SCRATCH_BYTES = 16 << 20
