@@ -19,7 +19,9 @@ the backward):
       + floor, sigma_r the standard deviation of the row's error in a
       first-order model of rounding at the input type (``rounding_sigma``).
   floor is 2^-12 of the head's RMS row norm (per row; sqrt(rows) of it per
-  tile).  (a) alone scales with the largest gradient of the head and cannot
+  tile); the per-tile floor adds a quarter of the rounding model's deviation
+  of the tile, so that a tile whose exact gradient vanishes (the naive
+  reference then has no error at all) is not failed on rounding noise.  (a) alone scales with the largest gradient of the head and cannot
   see rows far below it.  (b) is the tight check: a tile's error sums
   thousands of independent roundings, so the ratio of two same-precision
   computations stays close to 1, and a 1 % error on one tile fails it.  A
@@ -107,6 +109,8 @@ TILE_ROWS = 128
 #: terms are near Gaussian, where 6 deviations are not reached in 10^8 rows).
 UNIT_ROUNDOFF = {"fp16": 2.0 ** -11, "bf16": 2.0 ** -8}
 ROW_SIGMAS = 6.0
+#: Share of the rounding model's deviation added to the per-tile floor.
+TILE_SIGMAS = 0.25
 #: Absolute floor, relative to the head's RMS row norm (rows whose exact
 #: gradient is zero, e.g. dQ of query 0 under the causal mask, where both
 #: sides return rounding noise).
@@ -212,7 +216,7 @@ def check_grads(dtype: str, got: dict, ref: dict, naive: dict, where, stats: dic
             sl = slice(t0, min(rows, t0 + TILE_ROWS))
             e_t = float(np.sqrt(e2_row[sl].sum()))
             n_t = float(np.sqrt(n2_row[sl].sum()))
-            f_t = floor * np.sqrt(sl.stop - sl.start)
+            f_t = floor * np.sqrt(sl.stop - sl.start) + TILE_SIGMAS * float(np.sqrt(np.sum(sigma[name][sl] ** 2)))
             stats["max_tile_frac_" + name] = max(stats.get("max_tile_frac_" + name, 0.0),
                                                  e_t / max(NAIVE_FACTOR * n_t + f_t, 1e-300))
             if e_t > NAIVE_FACTOR * n_t + f_t:

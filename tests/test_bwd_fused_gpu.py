@@ -138,7 +138,7 @@ def test_errors_and_auto_selection():
     x = W.make_inputs(w, device="cuda")
     o, lse = fa.attention_forward(x["q"], x["k"], x["v"], w.sm_scale, w.causal)
     small = fa.fa_bwd_workspace_bytes_path(1, 2, 256, 256, 64, fa.FA_BWD_PATH_TWO_PASS)
-    assert fa.fa_bwd_workspace_bytes_path(1, 2, 256, 256, 64, fa.FA_BWD_PATH_FUSED) == small // 8 * (2 + 64)
+    assert fa.fa_bwd_workspace_bytes_path(1, 2, 256, 256, 64, fa.FA_BWD_PATH_FUSED) == small // 8 * 4 * (2 + 64)
     ws = torch.empty(small, dtype=torch.uint8, device="cuda")
     out = {n: torch.empty_like(x[s]) for n, s in (("dq", "q"), ("dk", "k"), ("dv", "v"))}
     with pytest.raises(fa.FaError) as e:

@@ -193,3 +193,17 @@ def test_a_second_same_precision_computation_passes(case):
     stats = {}
     check_grads(w.dtype, got, exact, naive, "tiled style", stats, sigma)
     print(case, {k: round(v, 3) for k, v in stats.items() if "frac" in k})
+
+
+def test_a_vanishing_gradient_with_rounding_noise_passes():
+    # One query and one key: dQ is exactly zero and so is the naive
+    # reference's error; a kernel's float32 noise there must pass, while a
+    # real error does not.
+    w, exact, naive, rounded, sigma = _setup(("bf16", 1, 1, 64, True, 1.0))
+    assert np.all(exact["dq"] == 0) and np.all(naive["dq"] == 0)
+    m = {n: a.copy() for n, a in rounded.items()}
+    m["dq"][0, :4] = 6e-8
+    check_grads(w.dtype, m, exact, naive, "noise", {}, sigma)
+    m["dv"] = -m["dv"]
+    with pytest.raises(AssertionError):
+        check_grads(w.dtype, m, exact, naive, "sign", {}, sigma)
