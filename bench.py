@@ -56,6 +56,9 @@ def parse_args(argv=None):
     ap.add_argument("--split", default="1", help="with --fwd-only: key-range splits (an integer, or 'auto')")
     ap.add_argument("--fp8v", action="store_true",
                     help="with --fwd-only: V in float8 e5m2, transposed, P cast to e5m2 (fa_fwd_fp8v)")
+    ap.add_argument("--bwd-only", action="store_true",
+                    help="time only the backward of --workload on --bwd-path, one JSON line")
+    ap.add_argument("--bwd-path", choices=["auto", "two_pass", "fused"], default="auto")
     ap.add_argument("--softmax", default=None, metavar="WORKLOAD",
                     help="time the row-softmax kernel on a named softmax workload instead, one JSON line")
     ap.add_argument("--source-hash", default=None, metavar="KERNEL",
@@ -629,6 +632,70 @@ def run_fwd_only(args):
         print(json.dumps(line), flush=True)
 
 
+def run_bwd_only(args):
+    """The backward alone (fa_bwd_ex, all three launches) of --workload on
+    --bwd-path: ms per backward, credited TFLOP/s (five products) and its
+    fraction of the tensor peak.  Inputs smaller than 256 MB are made cold by
+    a 256 MB write between calls, outside the timed launches."""
+    import torch
+
+    from tiled_attention_07_gb300 import fa
+    from tiled_attention_07_gb300 import workloads as W
+
+    rank, world = dist_init("nccl")
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = pick_workload(args)
+    path = {"auto": fa.FA_BWD_PATH_AUTO, "two_pass": fa.FA_BWD_PATH_TWO_PASS, "fused": fa.FA_BWD_PATH_FUSED}[
+        args.bwd_path]
+    x = {k: t.to(dev) for k, t in W.make_inputs(w, device="cpu", with_grad_output=True).items()}
+    stream = torch.cuda.current_stream(dev)
+    o = torch.empty_like(x["q"])
+    lse = torch.empty(fa.lse_shape(x["q"]), dtype=torch.float32, device=dev)
+    fa.fa_fwd(x["q"], x["k"], x["v"], o, lse, w.sm_scale, w.causal, stream)
+    g = {n: torch.empty_like(x[src]) for n, src in (("dq", "q"), ("dk", "k"), ("dv", "v"))}
+    B, H, Nq, d = fa._dims(x["q"])
+    Nk = fa._dims(x["k"])[2]
+    ws = torch.empty(max(fa.fa_bwd_workspace_bytes_path(B, H, Nq, Nk, d, path), 16), dtype=torch.uint8, device=dev)
+    in_bytes = sum(t.numel() * t.element_size() for t in x.values())
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if in_bytes < (256 << 20) else None
+
+    def run():
+        fa.fa_bwd_ex(path, 0, x["q"], x["k"], x["v"], o, x["do"], lse, g["dq"], g["dk"], g["dv"], w.sm_scale,
+                     w.causal, ws, stream)
+
+    clocks = ClockSampler() if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    barrier()
+    ms = reduce_max(time_forward(run, stream, args.steps, args.warmup, flush), dev)
+    barrier()
+    clk = clocks.stop() if clocks else None
+    rc, detail = fa.fa_last_device_error(stream)
+    if rc != fa.FA_OK:
+        raise RuntimeError(f"device error: {detail:#x}")
+    peaks, peak_src = load_peaks()
+    peak, peak_note = tensor_peak(peaks, peak_src, clk)
+    tf = w.bwd_flops() / (ms / 1e3) / 1e12
+    line = {
+        "metric": "attention backward TFLOP/s (credited: five products) on 1 GB300", "value": round(world * tf, 2),
+        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": w.dtype, "data": "synthetic (seeded q, k, v, dO)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": w.causal,
+                   "bwd_path": args.bwd_path, "flops_per_step": w.bwd_flops(),
+                   "l2": "256 MB scratch write between steps" if flush is not None else "inputs larger than L2",
+                   "parallelism": f"replica x{world}"},
+        "roofline": {"bound": "tensor", "kernel": "bwd (all launches)", "achieved": round(tf, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(tf / peak, 4), "traffic": None, "peak_source": peak_note},
+        "clocks": clk, "gpu_launches": 3 * args.steps, "e2e": None, "cpu_baseline": None,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_softmax(args):
     """fa_softmax_rows on one of the named row-softmax workloads: GB/s of the
     algorithmic bytes (every element read once and written once) against
@@ -871,6 +938,8 @@ def main(argv=None):
         run_reference(args)
     elif args.fwd_only:
         run_fwd_only(args)
+    elif args.bwd_only:
+        run_bwd_only(args)
     elif args.softmax:
         run_softmax(args)
     else:
