@@ -311,6 +311,19 @@ bool make_tile_map(CUtensorMap* map, const Tensor4& t, int d, int rows, int H, i
   return r == CUDA_SUCCESS;
 }
 
+bool make_f32_rows_map(CUtensorMap* map, const float* base, int64_t rows, int cols) {
+  EncodeTiledFn enc = get_encode();
+  if (enc == nullptr || rows <= 0 || cols <= 0 || (cols * 4) % 16 != 0) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 4};
+  const cuuint32_t box[2] = {32, static_cast<cuuint32_t>(kTileRows)};
+  const cuuint32_t estride[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estride,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool make_vt_map(CUtensorMap* map, const void* vt, int64_t ld, int Nk, int d, int H, int B) {
   EncodeTiledFn enc = get_encode();
   if (enc == nullptr) return false;

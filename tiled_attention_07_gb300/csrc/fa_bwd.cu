@@ -277,14 +277,16 @@ __device__ __forceinline__ void store16(uint8_t* dst, const uint32_t (&v)[16], f
 // FUSED (d = 64): also dQ.  The elementwise warps write dS_i = (dS^T_i)^T
 // into a shared-memory tile (keys x queries) besides the 16-bit dS^T in
 // TMEM; issuer B computes dQ_i = dS_i K into the last 64 TMEM columns (lanes
-// = queries), and the elementwise warps add that into the float32
-// accumulator during the next step (red.global.add), then release the
-// columns.  The dS tile is rewritten only after dQ_i has completed.
+// = queries).  During the next step the elementwise warps copy dQ_i into the
+// same shared tile (free once dQ_i has completed) as two 32-column float32
+// boxes in the 128-byte swizzle, and one more warp adds them into the
+// float32 accumulator with TMA tensor reductions (cp.reduce.async.bulk
+// .tensor .add); the tile takes dS_{i+1} once the TMA has read them.
 template <int D, bool BF16, bool FUSED = false>
-__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
+__global__ void __launch_bounds__(BwdCfg<D>::THREADS + (FUSED ? 32 : 0), 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                const MainParams p) {
+                const __grid_constant__ CUtensorMap tmAcc, const MainParams p) {
   using C = BwdCfg<D>;
   constexpr int NS = FUSED ? C::KVQ_NSTAGE : C::KV_NSTAGE;
   // kSepP: P^T has a 64-column region of its own (see above).
@@ -318,7 +320,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
   uint64_t* bar_ext = bar_dvd + 1;      // folded columns of K, V, Q_0, dO_0 written (kFold)
   uint64_t* bar_dq = bar_ext + 1;       // FUSED: dQ_i complete
   uint64_t* bar_dqfree = bar_dq + 1;    // FUSED: dQ_i read out of TMEM (one arrival per elementwise warp)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_dqfree + 1);
+  uint64_t* bar_stage = bar_dqfree + 1;  // FUSED: dQ_i staged in the shared tile (one arrival per elementwise warp)
+  uint64_t* bar_dsfree = bar_stage + 1;  // FUSED: the TMA has read the staged dQ_i
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_dsfree + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -351,6 +355,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     mbar_init(bar_ext, C::EW_WARPS);
     mbar_init(bar_dq, 1);
     mbar_init(bar_dqfree, C::EW_WARPS);
+    mbar_init(bar_stage, C::EW_WARPS);
+    mbar_init(bar_dsfree, 1);
     fence_mbar_init();
   }
   if (warp == C::MMA_WARP) {
@@ -394,6 +400,26 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       for (int it = max(0, n_issued - NS); it < n_issued; ++it) mbar_wait_drain(&bar_full[it % NS], (it / NS) & 1);
       mbar_wait_drain(bar_kv, 0);
     }
+  } else if (FUSED && warp == C::MMA_WARP + 2) {
+    // FUSED: the accumulator's reductions.  For each query tile, once the
+    // elementwise warps have staged dQ_i, add its two 32-column boxes into
+    // rows [bh Nqp + q0_i, + 128) of the accumulator; when the TMA has read
+    // them, hand the shared tile back for dS_{i+1}.  Every reduction has
+    // completed before the warp leaves.
+    const int row0 = bh * p.Nqp + i_first * kT;
+    for (int it = 0; it < n_it; ++it) {
+      mbar_wait(bar_stage, it & 1, p.err, 54);
+      if (elect_one()) {
+        tma_reduce_add_2d(&tmAcc, sDS, 0, row0 + it * kT);
+        tma_reduce_add_2d(&tmAcc, sDS + TileGeo<128>::CHB, 32, row0 + it * kT);
+        bulk_commit_group();
+        bulk_wait_group_read0();
+        mbar_arrive(bar_dsfree);
+      }
+      __syncwarp();
+    }
+    if (elect_one()) bulk_wait_group0();
+    __syncwarp();
   } else if (warp >= C::MMA_WARP) {
     // Two issuers: A (warp 9) computes S^T_i and dV, B (warp 10) dP^T_i and
     // dK, so that one issuer's barrier polls are covered by the other's MMAs.
@@ -484,10 +510,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
     const uint64_t cs2 = f2pack(p.scale_log2, p.scale_log2);
     const int kr = quad * 32 + lane;   // this thread's row of the K/V tile and of the stage rows it folds
 
-    // FUSED: add dQ_j (TMEM lanes = the 128 queries of query tile j) into the
-    // accumulator.  Warp (g, quad) takes lanes [32 quad, 32 quad + 32) and
-    // columns [16 g, 16 g + 16): four 16-byte reductions per thread.
-    auto reduce_dq = [&](int j) {
+    // FUSED: stage dQ_j (TMEM lanes = the 128 queries of query tile j) in the
+    // shared tile, which dQ_j, its last reader, has finished with: row r of
+    // box b (columns [32 b, 32 b + 32)) at b * 16 KB + r * 128 bytes, 16-byte
+    // granule x at x ^ (r % 8) (the 128-byte swizzle of the accumulator's
+    // tensor map).  Warp (g, quad) writes rows [32 quad, + 32), columns
+    // [16 g, + 16): box g / 2, granules 4 (g % 2) .. + 3.
+    auto stage_dq = [&](int j) {
       mbar_wait(bar_dq, j & 1, p.err, 53);
       tc_fence_after();
       uint32_t v[16];
@@ -496,11 +525,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_dqfree);
-      float* dst = p.dqacc + (static_cast<size_t>(bh) * p.Nqp + (i_first + j) * kT + quad * 32 + lane) * D + g * 16;
+      const int r = quad * 32 + lane;
+      uint8_t* row = sDS + (g >> 1) * TileGeo<128>::CHB + r * 128;
 #pragma unroll
       for (int c = 0; c < 4; ++c)
-        red_add_f32x4(dst + 4 * c, __uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
-                      __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]));
+        *reinterpret_cast<uint4*>(row + ((((g & 1) * 4 + c) ^ (r & 7)) << 4)) =
+            make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_stage);
     };
     // Folded columns of stage s: Q rows by warpgroup 2 (-L log2 e / c), dO
     // rows by warpgroup 3 (-D); L and D come with the stage.
@@ -596,7 +629,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_pt);
 
-      if (FUSED && it > 0) reduce_dq(it - 1);
+      if (FUSED && it > 0) stage_dq(it - 1);
 
       mbar_wait(bar_dp, it & 1, p.err, 29);
       tc_fence_after();
@@ -630,8 +663,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
         if constexpr (FUSED) {
           // dS_i row kr (this thread's key), queries [32 g, 32 g + 32): 64
           // bytes of 64-query chunk g / 2, 16-byte granules 4 (g % 2) .. + 3,
-          // 128-byte swizzle.  dQ_{i-1}, the last reader of the tile, has
-          // completed (reduce_dq waited for it).
+          // 128-byte swizzle.  The tile's last reader before this was the
+          // TMA reduction of the staged dQ_{i-1}.
+          if (it > 0) mbar_wait(bar_dsfree, (it - 1) & 1, p.err, 55);
           uint8_t* row = sDS + (g >> 1) * TileGeo<128>::CHB + kr * 128;
 #pragma unroll
           for (int c = 0; c < 4; ++c)
@@ -645,7 +679,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ds);
     }
-    if (FUSED && n_it > 0) reduce_dq(n_it - 1);
+    if (FUSED && n_it > 0) stage_dq(n_it - 1);
 
     // epilogue: warpgroups 0-1 write dV, 2-3 write dK * sm_scale (16-column
     // chunks alternate between the two warpgroups of each)
@@ -1028,10 +1062,11 @@ cudaError_t launch_bwd_t(const BwdArgs& a, int phase, cudaStream_t stream) {
   }
 
   if (phase == 1) return cudaSuccess;
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tacc = {};
   if (!make_tile_map(&tq, a.q, D, a.Nq, a.H, a.B, BF16) || !make_tile_map(&tk, a.k, D, a.Nk, a.H, a.B, BF16) ||
       !make_tile_map(&tv, a.v, D, a.Nk, a.H, a.B, BF16) || !make_tile_map(&tdo, a.dout, D, a.Nq, a.H, a.B, BF16))
     return cudaErrorInvalidValue;
+  if (a.fused && !make_f32_rows_map(&tacc, dqacc, static_cast<int64_t>(BH) * Nqp, D)) return cudaErrorInvalidValue;
 
   MainParams mp;
   mp.B = a.B;
@@ -1063,7 +1098,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, int phase, cudaStream_t stream) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::KVQ_SMEM);
         if (e != cudaSuccess) return e;
         const long long blocks = static_cast<long long>((a.Nk + kT - 1) / kT) * BH;
-        kern<<<static_cast<unsigned>(blocks), C::THREADS, C::KVQ_SMEM, stream>>>(tq, tk, tv, tdo, mp);
+        kern<<<static_cast<unsigned>(blocks), C::THREADS + 32, C::KVQ_SMEM, stream>>>(tq, tk, tv, tdo, tacc, mp);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
       }
@@ -1093,7 +1128,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, int phase, cudaStream_t stream) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::KV_SMEM);
     if (e != cudaSuccess) return e;
     const long long blocks = static_cast<long long>((a.Nk + kT - 1) / kT) * BH;
-    kern<<<static_cast<unsigned>(blocks), C::THREADS, C::KV_SMEM, stream>>>(tq, tk, tv, tdo, mp);
+    kern<<<static_cast<unsigned>(blocks), C::THREADS, C::KV_SMEM, stream>>>(tq, tk, tv, tdo, tacc, mp);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

@@ -94,6 +94,10 @@ bool make_tile_map(CUtensorMap* map, const Tensor4& t, int d, int rows, int H, i
 // 128-byte swizzle) by d rows.
 bool make_vt_map(CUtensorMap* map, const void* vt, int64_t ld, int Nk, int d, int H, int B);
 
+// Tensor map of a float32 [rows, cols] row-major matrix (cols * 4 bytes a
+// multiple of 16) with 32-column x 128-row boxes and the 128-byte swizzle.
+bool make_f32_rows_map(CUtensorMap* map, const float* base, int64_t rows, int cols);
+
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 // phase: 0 = all three launches; 1 = D / log2-LSE preprocess; 2 = dK, dV;
 // 3 = dQ (phases 2 and 3 read what phase 1 wrote to the workspace).  With

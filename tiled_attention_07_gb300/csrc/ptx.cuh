@@ -142,6 +142,19 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, const void*
       : "memory");
 }
 
+// 2-D tile reduction shared -> global: the box at coordinates (c0, c1) of
+// the tensor map's global tensor += the box in shared memory (element-wise
+// add in the map's element type, performed in L2), tracked by the issuing
+// thread's bulk async-group.  c0 * element size must be a multiple of 16
+// bytes and both coordinates non-negative.
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const void* src, int c0, int c1) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
 // 1-D bulk copy shared -> global (16-byte aligned addresses, size % 16 == 0),
 // tracked by the issuing thread's bulk async-group.
 __device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
@@ -311,6 +324,16 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
 }
 
+// 16 lanes x 256 bits, two 256-bit column blocks (shape 16x256b, .x2): thread
+// t holds lane (t / 4) in r[0], r[1] and lane (t / 4 + 8) in r[2], r[3] at
+// columns 2 (t % 4) + {0, 1}; r[4..7] the same for columns 8 + 2 (t % 4) +
+// {0, 1}.  Four threads together hold 8 consecutive columns of a lane.
+__device__ __forceinline__ void tmem_ld_16x256b_x2(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
@@ -360,6 +383,12 @@ __device__ __forceinline__ void tmem_reg_tie(uint32_t (&r)[32]) {
 // ---------------------------------------------------------------------------
 // Reductions into global memory
 // ---------------------------------------------------------------------------
+// [addr, addr + 8) += (a, b), float32, performed in L2 (no return value);
+// addr 8-byte aligned.
+__device__ __forceinline__ void red_add_f32x2(float* addr, float a, float b) {
+  asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(addr), "f"(a), "f"(b) : "memory");
+}
+
 // [addr, addr + 16) += (a, b, c, d), float32, performed in L2 (no return
 // value); addr 16-byte aligned.
 __device__ __forceinline__ void red_add_f32x4(float* addr, float a, float b, float c, float d) {
