@@ -108,7 +108,11 @@ def test_persistent_units(case):
     for n in ("dq", "dk", "dv"):
         assert torch.isfinite(grads[n]).all(), n
     grads2 = run_fwd_bwd(w, x)
-    for n in ("dq", "dk", "dv"):
+    # run to run: bitwise on the two-pass path; the fused path (taken where
+    # the workspace size says so) sums dQ's float32 shares in varying order
+    two_pass = fa.fa_bwd_workspace_bytes(B, H, Nq, Nk, d) == fa.fa_bwd_workspace_bytes_path(
+        B, H, Nq, Nk, d, fa.FA_BWD_PATH_TWO_PASS)
+    for n in ("dq", "dk", "dv") if two_pass else ("dk", "dv"):
         assert torch.equal(grads[n], grads2[n]), n
     print(w.name, stats)
 

@@ -149,11 +149,12 @@ struct BwdCfg {
   static constexpr int KV_NSTAGE = D == 64 ? 5 : (D == 80 ? 3 : 2);
   static constexpr int KV_STAGE = 2 * TILE + 2 * 512;
   static constexpr int KV_SMEM = 1024 + 2 * TILE + KV_NSTAGE * KV_STAGE + 512;
-  // fused dK/dV/dQ (d = 64): one ring stage less than dK/dV alone, to make
-  // room for the 128 x 128 16-bit dS tile
-  static constexpr int KVQ_NSTAGE = KV_NSTAGE - 1;
+  // fused dK/dV/dQ (d = 64): two ring stages less than dK/dV alone, to make
+  // room for the 128 x 128 16-bit dS tile and the 128 x 64 float32 dQ tile
+  static constexpr int KVQ_NSTAGE = KV_NSTAGE - 2;
   static constexpr int DS_TILE = 128 * 128 * 2;
-  static constexpr int KVQ_SMEM = 1024 + 2 * TILE + KVQ_NSTAGE * KV_STAGE + DS_TILE + 512;
+  static constexpr int DQ_TILE = 128 * D * 4;
+  static constexpr int KVQ_SMEM = 1024 + 2 * TILE + KVQ_NSTAGE * KV_STAGE + DS_TILE + DQ_TILE + 512;
   // dQ: Q, dO resident; ring of (K_j, V_j)
   static constexpr int Q_NSTAGE = D == 64 ? 5 : (D == 80 ? 3 : 2);
   static constexpr int Q_STAGE = 2 * TILE;
@@ -277,11 +278,10 @@ __device__ __forceinline__ void store16(uint8_t* dst, const uint32_t (&v)[16], f
 // FUSED (d = 64): also dQ.  The elementwise warps write dS_i = (dS^T_i)^T
 // into a shared-memory tile (keys x queries) besides the 16-bit dS^T in
 // TMEM; issuer B computes dQ_i = dS_i K into the last 64 TMEM columns (lanes
-// = queries).  During the next step the elementwise warps copy dQ_i into the
-// same shared tile (free once dQ_i has completed) as two 32-column float32
-// boxes in the 128-byte swizzle, and one more warp adds them into the
-// float32 accumulator with TMA tensor reductions (cp.reduce.async.bulk
-// .tensor .add); the tile takes dS_{i+1} once the TMA has read them.
+// = queries).  At the end of the next step the elementwise warps copy dQ_i
+// into a float32 tile of its own as two 32-column boxes in the 128-byte
+// swizzle, and one more warp adds them into the float32 accumulator with TMA
+// tensor reductions (cp.reduce.async.bulk.tensor .add).
 template <int D, bool BF16, bool FUSED = false>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS + (FUSED ? 32 : 0), 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -305,7 +305,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS + (FUSED ? 32 : 0), 1)
   uint8_t* sV = smem + C::TILE;
   uint8_t* sStage = smem + 2 * C::TILE;   // per stage: Q, dO, L[128], D[128]
   uint8_t* sDS = sStage + NS * C::KV_STAGE;   // FUSED: dS_i, 128 keys x 128 queries, two 64-query chunks
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sDS + (FUSED ? C::DS_TILE : 0));
+  uint8_t* sDQ = sDS + C::DS_TILE;            // FUSED: dQ_i, float32, two 32-column boxes
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sDS + (FUSED ? C::DS_TILE + C::DQ_TILE : 0));
   uint64_t* bar_kv = bars;            // K, V loaded
   uint64_t* bar_full = bars + 1;      // [NS]
   uint64_t* bar_empty = bar_full + NS;
@@ -320,8 +321,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS + (FUSED ? 32 : 0), 1)
   uint64_t* bar_ext = bar_dvd + 1;      // folded columns of K, V, Q_0, dO_0 written (kFold)
   uint64_t* bar_dq = bar_ext + 1;       // FUSED: dQ_i complete
   uint64_t* bar_dqfree = bar_dq + 1;    // FUSED: dQ_i read out of TMEM (one arrival per elementwise warp)
-  uint64_t* bar_stage = bar_dqfree + 1;  // FUSED: dQ_i staged in the shared tile (one arrival per elementwise warp)
-  uint64_t* bar_dsfree = bar_stage + 1;  // FUSED: the TMA has read the staged dQ_i
+  uint64_t* bar_stage = bar_dqfree + 1;  // FUSED: dQ_i staged in its shared tile (one arrival per elementwise warp)
+  uint64_t* bar_dsfree = bar_stage + 1;  // FUSED: the TMA has read the staged dQ_i (the tile may be reused)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_dsfree + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -404,14 +405,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS + (FUSED ? 32 : 0), 1)
     // FUSED: the accumulator's reductions.  For each query tile, once the
     // elementwise warps have staged dQ_i, add its two 32-column boxes into
     // rows [bh Nqp + q0_i, + 128) of the accumulator; when the TMA has read
-    // them, hand the shared tile back for dS_{i+1}.  Every reduction has
-    // completed before the warp leaves.
+    // them, hand the tile back for dQ_{i+1}.  Every reduction has completed
+    // before the warp leaves.
     const int row0 = bh * p.Nqp + i_first * kT;
     for (int it = 0; it < n_it; ++it) {
       mbar_wait(bar_stage, it & 1, p.err, 54);
       if (elect_one()) {
-        tma_reduce_add_2d(&tmAcc, sDS, 0, row0 + it * kT);
-        tma_reduce_add_2d(&tmAcc, sDS + TileGeo<128>::CHB, 32, row0 + it * kT);
+        tma_reduce_add_2d(&tmAcc, sDQ, 0, row0 + it * kT);
+        tma_reduce_add_2d(&tmAcc, sDQ + 128 * 128, 32, row0 + it * kT);
         bulk_commit_group();
         bulk_wait_group_read0();
         mbar_arrive(bar_dsfree);
@@ -510,9 +511,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS + (FUSED ? 32 : 0), 1)
     const uint64_t cs2 = f2pack(p.scale_log2, p.scale_log2);
     const int kr = quad * 32 + lane;   // this thread's row of the K/V tile and of the stage rows it folds
 
-    // FUSED: stage dQ_j (TMEM lanes = the 128 queries of query tile j) in the
-    // shared tile, which dQ_j, its last reader, has finished with: row r of
-    // box b (columns [32 b, 32 b + 32)) at b * 16 KB + r * 128 bytes, 16-byte
+    // FUSED: stage dQ_j (TMEM lanes = the 128 queries of query tile j) in
+    // its shared tile once the TMA has read dQ_{j-1} from it: row r of box b
+    // (columns [32 b, 32 b + 32)) at b * 16 KB + r * 128 bytes, 16-byte
     // granule x at x ^ (r % 8) (the 128-byte swizzle of the accumulator's
     // tensor map).  Warp (g, quad) writes rows [32 quad, + 32), columns
     // [16 g, + 16): box g / 2, granules 4 (g % 2) .. + 3.
@@ -525,8 +526,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS + (FUSED ? 32 : 0), 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_dqfree);
+      if (j > 0) mbar_wait(bar_dsfree, (j - 1) & 1, p.err, 55);
       const int r = quad * 32 + lane;
-      uint8_t* row = sDS + (g >> 1) * TileGeo<128>::CHB + r * 128;
+      uint8_t* row = sDQ + (g >> 1) * (128 * 128) + r * 128;
 #pragma unroll
       for (int c = 0; c < 4; ++c)
         *reinterpret_cast<uint4*>(row + ((((g & 1) * 4 + c) ^ (r & 7)) << 4)) =
@@ -629,8 +631,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS + (FUSED ? 32 : 0), 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_pt);
 
-      if (FUSED && it > 0) stage_dq(it - 1);
-
       mbar_wait(bar_dp, it & 1, p.err, 29);
       tc_fence_after();
       {
@@ -663,9 +663,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS + (FUSED ? 32 : 0), 1)
         if constexpr (FUSED) {
           // dS_i row kr (this thread's key), queries [32 g, 32 g + 32): 64
           // bytes of 64-query chunk g / 2, 16-byte granules 4 (g % 2) .. + 3,
-          // 128-byte swizzle.  The tile's last reader before this was the
-          // TMA reduction of the staged dQ_{i-1}.
-          if (it > 0) mbar_wait(bar_dsfree, (it - 1) & 1, p.err, 55);
+          // 128-byte swizzle.  The tile's last reader was dQ_{i-1}.
+          if (it > 0) {
+            mbar_wait(bar_dq, (it - 1) & 1, p.err, 56);
+            tc_fence_after();
+          }
           uint8_t* row = sDS + (g >> 1) * TileGeo<128>::CHB + kr * 128;
 #pragma unroll
           for (int c = 0; c < 4; ++c)
@@ -678,6 +680,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS + (FUSED ? 32 : 0), 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ds);
+      if (FUSED && it > 0) stage_dq(it - 1);
     }
     if (FUSED && n_it > 0) stage_dq(n_it - 1);
 
