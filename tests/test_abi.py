@@ -150,9 +150,12 @@ def test_bwd_phase_rejects_unknown_phase(L):
 
 
 def test_bwd_checks_workspace_and_args(L):
-    need = fa.fa_bwd_workspace_bytes(1, 1, 128, 128, 64)
+    # below the two-pass size is too small for every path (a workspace of the
+    # fused size less a little only makes AUTO take the two-pass path)
+    need = fa.fa_bwd_workspace_bytes_path(1, 1, 128, 128, 64, fa.FA_BWD_PATH_TWO_PASS)
     assert bwd(L, ws=None) == fa.FA_ERR_WORKSPACE
     assert bwd(L, ws_bytes=need - 16) == fa.FA_ERR_WORKSPACE
+    assert bwd(L, d=80, ws_bytes=fa.fa_bwd_workspace_bytes(1, 1, 128, 128, 80) - 16) == fa.FA_ERR_WORKSPACE
     assert bwd(L, ws=FAKE + 4) == fa.FA_ERR_WORKSPACE
     assert bwd(L, d=100) == fa.FA_ERR_UNSUPPORTED
     assert bwd(L, Nk=0) == fa.FA_ERR_INVALID_ARG
@@ -289,3 +292,34 @@ def test_softmax_span_overflow_is_rejected(L):
                              None) == fa.FA_ERR_INVALID_ARG
     assert L.fa_softmax_rows(FAKE, FAKE + (1 << 24), None, 2, 128, 2 ** 62, 128, fa.FA_FP32,
                              None) == fa.FA_ERR_INVALID_ARG
+
+
+def test_bwd_path_workspace_bytes(lib):
+    rows = 4 * 20 * 4096
+    two = fa.fa_bwd_workspace_bytes_path(4, 20, 4096, 4096, 64, fa.FA_BWD_PATH_TWO_PASS)
+    fused = fa.fa_bwd_workspace_bytes_path(4, 20, 4096, 4096, 64, fa.FA_BWD_PATH_FUSED)
+    assert two == 8 * rows and fused == 4 * (2 + 64) * rows
+    # AUTO prefers the fused path at d = 64 and the two-pass path elsewhere
+    assert fa.fa_bwd_workspace_bytes(4, 20, 4096, 4096, 64) == fused
+    assert fa.fa_bwd_workspace_bytes_path(4, 20, 4096, 4096, 64, fa.FA_BWD_PATH_AUTO) == fused
+    assert fa.fa_bwd_workspace_bytes(4, 32, 8192, 8192, 80) == 8 * 4 * 32 * 8192
+    for d in (80, 128):
+        assert fa.fa_bwd_workspace_bytes_path(1, 2, 300, 300, d, fa.FA_BWD_PATH_FUSED) == 0
+    assert fa.fa_bwd_workspace_bytes_path(1, 2, 0, 300, 64, fa.FA_BWD_PATH_FUSED) == 0
+    assert fa.fa_bwd_workspace_bytes_path(1, 2, 300, 300, 64, 7) == 0
+
+
+def test_bwd_ex_rejects_bad_path_phase_and_size(L):
+    ptrs = [FAKE] * 9
+
+    def ex(path, phase=0, d=64, ws_bytes=1 << 30):
+        return L.fa_bwd_ex(path, phase, *ptrs, 1, 1, 128, 128, d, 0.125, 0, fa.FA_BF16, None, FAKE, ws_bytes, None)
+
+    assert ex(3) == fa.FA_ERR_INVALID_ARG
+    assert ex(-1) == fa.FA_ERR_INVALID_ARG
+    for phase in (4, -1):
+        assert ex(fa.FA_BWD_PATH_FUSED, phase) == fa.FA_ERR_INVALID_ARG
+    assert ex(fa.FA_BWD_PATH_FUSED, d=80) == fa.FA_ERR_UNSUPPORTED
+    two = fa.fa_bwd_workspace_bytes_path(1, 1, 128, 128, 64, fa.FA_BWD_PATH_TWO_PASS)
+    assert ex(fa.FA_BWD_PATH_FUSED, ws_bytes=two) == fa.FA_ERR_WORKSPACE
+    assert ex(fa.FA_BWD_PATH_TWO_PASS, ws_bytes=two - 16) == fa.FA_ERR_WORKSPACE

@@ -88,7 +88,8 @@ def test_noalloc_at_the_scratch_limit_allocates_nothing():
     # problem stays small in time.
     rows = fa.NOALLOC_SCRATCH_BYTES // 8
     w = W.custom("bf16", "bhsd", 2, 8, rows // 16, 128, 64, False, seed=73, backward=True)
-    assert fa.fa_bwd_workspace_bytes(w.B, w.H, w.Nq, w.Nk, w.d) == fa.NOALLOC_SCRATCH_BYTES
+    assert fa.fa_bwd_workspace_bytes_path(w.B, w.H, w.Nq, w.Nk, w.d,
+                                          fa.FA_BWD_PATH_TWO_PASS) == fa.NOALLOC_SCRATCH_BYTES
     x = W.make_inputs(w, device="cuda")
     o, lse = fa.attention_forward(x["q"], x["k"], x["v"], w.sm_scale, w.causal)
     # fa_bwd_noalloc always takes the two-pass backward: the same path through
