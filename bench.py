@@ -56,6 +56,8 @@ def parse_args(argv=None):
     ap.add_argument("--split", default="1", help="with --fwd-only: key-range splits (an integer, or 'auto')")
     ap.add_argument("--fp8v", action="store_true",
                     help="with --fwd-only: V in float8 e5m2, transposed, P cast to e5m2 (fa_fwd_fp8v)")
+    ap.add_argument("--fp8v-lazy", action="store_true",
+                    help="with --fp8v: the lazy running-max rule (FA_FP8V_LAZY_MAX) instead of the page's steps")
     ap.add_argument("--bwd-only", action="store_true",
                     help="time only the backward of --workload on --bwd-path, one JSON line")
     ap.add_argument("--bwd-path", choices=["auto", "two_pass", "fused"], default="auto")
@@ -558,7 +560,8 @@ def run_fwd_only(args):
 
     def fwd():
         if args.fp8v:
-            fa.fa_fwd_fp8v(q, k, v, o, lse, w.sm_scale, w.causal, stream)
+            fa.fa_fwd_fp8v(q, k, v, o, lse, w.sm_scale, w.causal, stream,
+                           mode=fa.FA_FP8V_LAZY_MAX if args.fp8v_lazy else fa.FA_FP8V_PAGE_STEPS)
         elif n_splits > 1:
             fa.fa_fwd_split(q, k, v, o, lse, w.sm_scale, w.causal, n_splits, ws, stream)
         else:
@@ -612,7 +615,7 @@ def run_fwd_only(args):
         "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": max(args.warmup, 3),
         "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": (w.dtype + " q,k,o; e5m2 v,p") if args.fp8v else w.dtype, "data": "synthetic (seeded q, k, v)",
-        "config": {"workload": w.name + ("_fp8v" if args.fp8v else ""), "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk,
+        "config": {"workload": w.name + (("_fp8v_lazy" if args.fp8v_lazy else "_fp8v") if args.fp8v else ""), "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk,
                    "d": w.d, "causal": w.causal, "layout": w.layout, "split": n_splits, "flops_per_step": flops,
                    "l2": "256 MB scratch write between steps" if flush is not None else "inputs larger than L2",
                    "parallelism": f"replica x{world}"},

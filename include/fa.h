@@ -176,8 +176,13 @@ FA_API fa_status fa_fwd_split(const void* q, const void* k, const void* v, void*
  * q, k and o are contiguous; dtype (FA_FP16 or FA_BF16) is theirs.  S = q k^T
  * runs on the 16-bit tensor-core path; P is rounded to e5m2 (to nearest
  * even, saturating) and O += P V runs on the 8-bit path (kind::f8f6f4) with
- * float32 accumulation.  LSE is exact, as in fa_fwd; O differs from the
- * exact result by at most about 2^-3 * max |v| over the row's keys (the
+ * float32 accumulation.  p is taken, per block of 128 keys, against the
+ * running max of the blocks so far, moved at every block as in the page's
+ * steps (O is rescaled in tensor memory whenever a row's max grows), so the
+ * kernel casts the same p as those steps; the float32 arithmetic that forms
+ * p can only move an element lying within about 1e-6 of an e5m2 rounding
+ * midpoint to the other side.  LSE is exact, as in fa_fwd; O differs from
+ * the exact result by at most about 2^-3 * max |v| over the row's keys (the
  * rounding of P, relative 2^-3) plus the 16-bit rounding of O.
  * d in {64, 80, 128} (at d = 128 the 8-bit P is written over the first 32
  * columns of its tile's S in tensor memory, as the 16-bit P is there).
@@ -187,6 +192,24 @@ FA_API fa_status fa_fwd_split(const void* q, const void* k, const void* v, void*
 FA_API fa_status fa_fwd_fp8v(const void* q, const void* k, const void* vt, void* o, float* lse,
                       int B, int H, int Nq, int Nk, int d, int64_t vt_ld, float sm_scale,
                       int causal, fa_dtype dtype, void* stream);
+
+/*
+ * fa_fwd_fp8v_ex -- fa_fwd_fp8v with a choice of running-max rule:
+ *   FA_FP8V_PAGE_STEPS (0): as fa_fwd_fp8v (the page's steps).
+ *   FA_FP8V_LAZY_MAX (1): the running max moves only when a row's max grows
+ *     by more than 2^8 (in log2 units), as in the 16-bit forward, so O is
+ *     rarely rescaled.  This departs from the page's steps: p is taken at a
+ *     scale up to 2^8 larger than theirs and its e5m2 rounding can differ by
+ *     one step, so O differs from theirs by up to about 2^-2 * max |v| over
+ *     the row's keys (and from the exact result by the same 2^-3 bound as
+ *     above).  Faster: the per-block rescale of O costs the page's rule
+ *     about 20 % of the forward on causal shapes.
+ * Other values of mode give FA_ERR_INVALID_ARG.
+ */
+enum { FA_FP8V_PAGE_STEPS = 0, FA_FP8V_LAZY_MAX = 1 };
+FA_API fa_status fa_fwd_fp8v_ex(const void* q, const void* k, const void* vt, void* o, float* lse,
+                         int B, int H, int Nq, int Nk, int d, int64_t vt_ld, float sm_scale,
+                         int causal, fa_dtype dtype, int mode, void* stream);
 
 /*
  * fa_bwd_workspace_bytes -- size of the scratch buffer fa_bwd needs: the

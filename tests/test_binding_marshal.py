@@ -127,8 +127,10 @@ def test_fp8v_forward_passes_the_row_length(lib):
     k = torch.zeros(B, H, Nk, d, dtype=BF)
     vt = torch.zeros(B, H, d, ld, dtype=torch.uint8)[..., :Nk]
     fa.fa_fwd_fp8v(q, k, vt, o, torch.zeros(B, H, Nq), 0.125, True)
-    a = last(lib, "fa_fwd_fp8v")
-    assert a[2] == vt.data_ptr() and a[5:11] == (B, H, Nq, Nk, d, ld)
+    a = last(lib, "fa_fwd_fp8v_ex")
+    assert a[2] == vt.data_ptr() and a[5:11] == (B, H, Nq, Nk, d, ld) and a[14] == fa.FA_FP8V_PAGE_STEPS
+    fa.fa_fwd_fp8v(q, k, vt, o, torch.zeros(B, H, Nq), 0.125, True, mode=fa.FA_FP8V_LAZY_MAX)
+    assert last(lib, "fa_fwd_fp8v_ex")[14] == fa.FA_FP8V_LAZY_MAX
 
 
 def test_softmax_rows_strides(lib):

@@ -3,17 +3,23 @@
 Two comparisons:
 
 * Tight, against the e5m2 oracle (oracle.fp8.forward_fp8v), with the
-  forward's tolerances.  The inputs put every row's largest score at key 0
-  (q = (1, r_i), k_0 = (a, 0, ...), k_j = (0, t_j)), so the running max is
-  final after the first key tile, on the GPU (which keeps its max unless it
-  grows) as in the oracle (which updates it every tile): both cast the same p
-  to e5m2.  Rows where a random score comes within 1e-3 of key 0's are left
-  out of this check (at least 90 % must remain).  The GPU result must also be
-  nearer the e5m2 oracle than the exact one, so the cast is really there.
+  forward's tolerances, on plain seeded random inputs, every row.  The
+  kernel takes p against the running max of the key blocks so far, moved at
+  every block, as the steps of "Understanding Triton Tutorials Part 2",
+  "Fused Attention 2" do, so both cast the same p to e5m2 (the float32
+  arithmetic that forms p on the GPU can only move an element lying within
+  about 1e-6 of an e5m2 rounding midpoint to the other side).  The GPU
+  result must also be nearer the e5m2 oracle than the exact one, so the
+  cast is really there.
 * Loose, against the exact oracle on plain random inputs: the cast of p
   (relative error <= 2^-3) bounds |O_gpu - O_exact| by 2^-3 max |v| over the
   row's visible keys, plus the 16-bit tolerance and half an output ulp; the
   LSE sums unrounded p and keeps the forward's LSE tolerance.
+
+The lazy running-max rule (FA_FP8V_LAZY_MAX) departs from the page's steps:
+it is held to the loose bound on random inputs, and to the e5m2 oracle on
+inputs built so that every row's largest score sits at key 0 (then both
+rules keep the max of the first block, and cast the same p).
 """
 
 import numpy as np
@@ -30,28 +36,15 @@ from parity import LSE_TOL, O_TOL, half_ulp, to64
 pytestmark = pytest.mark.gpu
 
 
-def run(w, x):
+def run(w, x, mode=fa.FA_FP8V_PAGE_STEPS):
     q, k, vt = x["q"], x["k"], x["vt"]
     o = torch.full_like(q, float("nan"))
     lse = torch.full(fa.lse_shape(q), float("nan"), dtype=torch.float32, device=q.device)
-    fa.fa_fwd_fp8v(q, k, vt, o, lse, w.sm_scale, w.causal)
+    fa.fa_fwd_fp8v(q, k, vt, o, lse, w.sm_scale, w.causal, mode=mode)
     torch.cuda.synchronize()
     rc, detail = fa.fa_last_device_error()
     assert rc == fa.FA_OK, f"device error {detail:#x}"
     return o, lse
-
-
-def key0_max_inputs(w, device="cuda", pad_code=0):
-    """fp8v_inputs with every row's largest score at key 0 (see above)."""
-    x = W.fp8v_inputs(w, "cpu", pad_code=pad_code)
-    q, k = x["q"].clone(), x["k"].clone()
-    a = 5.0 / w.sm_scale
-    q[..., 0] = 1.0
-    k[..., 0] = 0.0
-    k[..., 0, :] = 0.0
-    k[..., 0, 0] = a
-    x["q"], x["k"] = q, k
-    return {n: t.to(device) for n, t in x.items()}
 
 
 def oracle_heads(w, x, heads, exact=False):
@@ -72,37 +65,48 @@ def heads_of(w, limit=4):
     return hs if len(hs) <= limit else [hs[0], hs[len(hs) // 2], hs[-1]]
 
 
-def check_tight(w):
-    x = key0_max_inputs(w)
-    o, lse = run(w, x)
+def key0_max_inputs(w, device="cuda"):
+    """fp8v_inputs with every row's largest score at key 0: q = (1, r_i),
+    k_0 = (a, 0, ...), k_j = (0, t_j)."""
+    x = W.fp8v_inputs(w, "cpu")
+    q, k = x["q"].clone(), x["k"].clone()
+    q[..., 0] = 1.0
+    k[..., 0] = 0.0
+    k[..., 0, :] = 0.0
+    k[..., 0, 0] = 5.0 / w.sm_scale
+    x["q"], x["k"] = q, k
+    return {n: t.to(device) for n, t in x.items()}
+
+
+def check_tight(w, mode=fa.FA_FP8V_PAGE_STEPS, key0=False):
+    x = key0_max_inputs(w) if key0 else W.fp8v_inputs(w, "cuda")
+    o, lse = run(w, x, mode)
     heads = heads_of(w)
     r8 = oracle_heads(w, x, heads)
     rx = oracle_heads(w, x, heads, exact=True)
-    kept = total = 0
     d8 = dx = 0.0
+    rows = 0
+    worst = 0.0
     for b, h in heads:
         o8, l8 = r8[(b, h)]
         ox, lx = rx[(b, h)]
         og = to64(o[b, h])
-        # rows whose maximum is key 0 by a margin
-        s = ref.scores(to64(x["q"][b, h]), to64(x["k"][b, h]), w.sm_scale, w.causal)
-        others = np.max(np.where(np.arange(s.shape[1])[None, :] == 0, -np.inf, s), axis=1)
-        rows = s[:, 0] > others + 1e-3
-        kept += int(rows.sum())
-        total += rows.size
-        err = np.abs(og - o8)[rows] - half_ulp(o8[rows], w.dtype)
+        err = np.abs(og - o8) - half_ulp(o8, w.dtype)
+        worst = max(worst, float(err.max()))
         assert err.max() <= O_TOL[w.dtype], f"head {(b, h)}: max |O - O_e5m2| excess {err.max():.3g}"
         assert np.abs(to64(lse[b, h]) - lx).max() <= LSE_TOL
-        d8 += float(np.sum((og - o8)[rows] ** 2))
-        dx += float(np.sum((og - ox)[rows] ** 2))
-    assert kept >= 0.9 * total, f"only {kept} of {total} rows have their maximum at key 0"
+        assert np.abs(to64(lse[b, h]) - l8).max() <= LSE_TOL
+        d8 += float(np.sum((og - o8) ** 2))
+        dx += float(np.sum((og - ox) ** 2))
+        rows += og.shape[0]
     assert d8 < 0.25 * dx, f"GPU not nearer the e5m2 oracle than the exact one ({d8:.3g} vs {dx:.3g})"
-    return {"rows": kept, "rms_vs_e5m2": (d8 / kept / w.d) ** 0.5, "rms_vs_exact": (dx / kept / w.d) ** 0.5}
+    return {"rows": rows, "max_excess_over_half_ulp": worst, "rms_vs_e5m2": (d8 / rows / w.d) ** 0.5,
+            "rms_vs_exact": (dx / rows / w.d) ** 0.5}
 
 
-def check_loose(w, pad_code=0):
+def check_loose(w, pad_code=0, mode=fa.FA_FP8V_PAGE_STEPS):
     x = W.fp8v_inputs(w, "cuda", pad_code=pad_code)
-    o, lse = run(w, x)
+    o, lse = run(w, x, mode)
     heads = heads_of(w)
     rx = oracle_heads(w, x, heads, exact=True)
     worst = 0.0
@@ -127,6 +131,9 @@ def check_loose(w, pad_code=0):
     ("fp16", 1, 2, 513, 700, 128, False),    # d = 128: P over the S columns
     ("fp16", 2, 1, 600, 600, 128, True),
     ("fp16", 1, 320, 512, 512, 80, True),    # enough heads for the work-unit blocks
+    ("bf16", 1, 2, 1024, 1024, 80, True),
+    ("bf16", 2, 160, 768, 768, 64, True),    # work-unit blocks, an odd middle pair
+    ("bf16", 2, 2, 129, 77, 64, True),       # one ragged key tile
 ])
 def test_tight_against_e5m2_oracle(dtype, B, H, Nq, Nk, d, causal):
     w = W.custom(dtype, "bhsd", B, H, Nq, Nk, d, causal, seed=Nq + Nk + d)
@@ -141,9 +148,21 @@ def test_tight_against_e5m2_oracle(dtype, B, H, Nq, Nk, d, causal):
     ("bf16", 1, 2, 1000, 1000, 128, True),
     ("bf16", 2, 160, 768, 768, 64, True),    # work-unit blocks, an odd middle pair
 ])
-def test_loose_against_exact(dtype, B, H, Nq, Nk, d, causal):
+@pytest.mark.parametrize("mode", [fa.FA_FP8V_PAGE_STEPS, fa.FA_FP8V_LAZY_MAX], ids=["page", "lazy"])
+def test_loose_against_exact(dtype, B, H, Nq, Nk, d, causal, mode):
     w = W.custom(dtype, "bhsd", B, H, Nq, Nk, d, causal, seed=3 * Nq + Nk)
-    print(w.name, check_loose(w))
+    print(w.name, check_loose(w, mode=mode))
+
+
+@pytest.mark.parametrize("dtype,B,H,Nq,Nk,d,causal", [
+    ("fp16", 1, 2, 700, 700, 80, True),
+    ("bf16", 1, 3, 640, 640, 64, True),
+    ("fp16", 2, 1, 600, 600, 128, True),
+    ("fp16", 1, 320, 512, 512, 80, True),
+])
+def test_lazy_mode_tight_where_the_first_block_holds_the_max(dtype, B, H, Nq, Nk, d, causal):
+    w = W.custom(dtype, "bhsd", B, H, Nq, Nk, d, causal, seed=Nq + Nk + d)
+    print(w.name, check_tight(w, mode=fa.FA_FP8V_LAZY_MAX, key0=True))
 
 
 def test_padding_bytes_are_not_read():

@@ -171,9 +171,11 @@ fa_status fwd_impl(const Tensor4& q, const Tensor4& k, const Tensor4& v, const T
 }
 
 fa_status fwd_fp8v_impl(const void* q, const void* k, const void* vt, void* o, float* lse, int B, int H, int Nq,
-                        int Nk, int d, int64_t ld, float sm_scale, int causal, fa_dtype dtype, void* stream) {
+                        int Nk, int d, int64_t ld, float sm_scale, int causal, fa_dtype dtype, void* stream,
+                        int mode = FA_FP8V_PAGE_STEPS) {
   fa_status st = check_common(B, H, Nq, Nk, d, sm_scale, causal, dtype);
   if (st != FA_OK) return st;
+  if (mode != FA_FP8V_PAGE_STEPS && mode != FA_FP8V_LAZY_MAX) return FA_ERR_INVALID_ARG;
   if (ld < Nk || ld % 16 != 0 || ld >= (int64_t(1) << 32)) return FA_ERR_INVALID_ARG;
   if (B == 0 || H == 0 || Nq == 0) return FA_OK;
   const Tensor4 tq = contiguous(q, H, Nq, d), tk = contiguous(k, H, Nk, d), to = contiguous(o, H, Nq, d);
@@ -206,6 +208,7 @@ fa_status fwd_fp8v_impl(const void* q, const void* k, const void* vt, void* o, f
   a.err = err;
   a.fp8v = true;
   a.vt_ld = ld;
+  a.fp8_lazy = mode == FA_FP8V_LAZY_MAX;
   e = launch_fwd(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -355,6 +358,12 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 fa_status fa_fwd_fp8v(const void* q, const void* k, const void* vt, void* o, float* lse, int B, int H, int Nq,
                       int Nk, int d, int64_t vt_ld, float sm_scale, int causal, fa_dtype dtype, void* stream) {
   return fa::fwd_fp8v_impl(q, k, vt, o, lse, B, H, Nq, Nk, d, vt_ld, sm_scale, causal, dtype, stream);
+}
+
+fa_status fa_fwd_fp8v_ex(const void* q, const void* k, const void* vt, void* o, float* lse, int B, int H, int Nq,
+                         int Nk, int d, int64_t vt_ld, float sm_scale, int causal, fa_dtype dtype, int mode,
+                         void* stream) {
+  return fa::fwd_fp8v_impl(q, k, vt, o, lse, B, H, Nq, Nk, d, vt_ld, sm_scale, causal, dtype, stream, mode);
 }
 
 fa_status fa_fwd_strided(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,

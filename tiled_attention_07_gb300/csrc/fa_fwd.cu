@@ -58,6 +58,15 @@ constexpr float kRescaleLog2 = 8.0f;
 // row by the same, i.e. its max grew by at most kRescaleLog2.
 constexpr float kFastSumBound = 256.0f;
 static_assert(kFastSumBound == (1 << static_cast<int>(kRescaleLog2)), "keep the two bounds in step");
+// How far a row's max may grow before the running max is moved: 2^8 with
+// 16-bit P (the stale max is exact, as O / l and LSE use the same one), and
+// with e5m2 P under the lazy rule (LAZY8); 0 with e5m2 P otherwise.  The
+// e5m2 cast of p depends on the scale p is taken at, and "Fused Attention 2"
+// takes p against the running max of the blocks so far, moved at every
+// block; the kernels do the same by default, so that they cast the same
+// values (O is then rescaled whenever a row's max grows).
+template <bool FP8V, bool LAZY8>
+constexpr float kMaxGrowth = FP8V && !LAZY8 ? 0.0f : kRescaleLog2;
 
 template <int D>
 struct FwdCfg {
@@ -242,7 +251,10 @@ __device__ __forceinline__ float exp_pack(const float (&s)[kBN], uint64_t cs2, u
   return a0 + a1;
 }
 
-template <int D, bool BF16, bool FP8V>
+// LAZY8 (e5m2 P only): the running max moves only when it grows by more
+// than 2^8, as with 16-bit P (faster; p's e5m2 cast can then differ from the
+// page's steps by one rounding step), instead of at every block.
+template <int D, bool BF16, bool FP8V, bool LAZY8 = false>
 __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -502,7 +514,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           tmem_st16(tS + i * 16, pk);
         }
         const float mx = fmax3(fmax3(mc[0], mc[1], mc[2]), fmax3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
-        const bool need = mx * cs > m + kRescaleLog2;
+        const bool need = mx * cs > m + kMaxGrowth<FP8V, LAZY8>;
         if (!__any_sync(0xffffffffu, need)) {
           float a0, a1;
           f2unpack(fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3])), a0, a1);
@@ -527,7 +539,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         if (j == 0) {
           m = m_tile;
         } else {
-          const bool need = m_tile > m + kRescaleLog2;
+          const bool need = m_tile > m + kMaxGrowth<FP8V, LAZY8>;
           const float m_new = need ? m_tile : m;
           const float alpha = ex2_approx(m - m_new);
           m = m_new;
@@ -735,7 +747,7 @@ struct FwdSpCfg {
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 
-template <int D, bool BF16, bool FP8V>
+template <int D, bool BF16, bool FP8V, bool LAZY8 = false>
 __global__ void __launch_bounds__(FwdSpCfg<D>::THREADS, 1)
     fwd_sp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -1001,7 +1013,31 @@ __global__ void __launch_bounds__(FwdSpCfg<D>::THREADS, 1)
         constexpr int NPK = FP8V ? kBN / 4 : kBN / 2;   // P registers (and TMEM columns) per row
         uint32_t pk[NPK];
         bool done = false;
-        if (j > 0) {
+        bool grew = false;   // FP8V: some row of this warp has a new max (O must be rescaled)
+        float alpha8 = 1.f;
+        if (FP8V && !LAZY8 && j > 0) {
+          // e5m2 P: the max first, then one pass against the new running max
+          // (the scale the page's steps take p at), O rescaled below if a
+          // row of this warp grew.
+          float mc[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mc[i] = fmaxf(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+          for (int c = 16; c < kBN; c += 16) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mc[i] = fmax3(mc[i], s[c + 2 * i], s[c + 2 * i + 1]);
+          }
+          const float mx = fmax3(fmax3(mc[0], mc[1], mc[2]), fmax3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
+          const float m_new = fmaxf(m, mx * cs);
+          alpha8 = m == -CUDART_INF_F ? 0.f : ex2_approx(m - m_new);
+          grew = __any_sync(0xffffffffu, m_new > m);
+          m = m_new;
+          const float mb = (m == -CUDART_INF_F) ? 0.f : m;
+          l = l * alpha8 + exp_pack<BF16, FP8V>(s, cs2, f2pack(-mb, -mb), pk);
+#pragma unroll
+          for (int i = 0; i < NPK / 32; ++i) tmem_reg_tie(*reinterpret_cast<uint32_t(*)[32]>(&pk[32 * i]));
+          done = true;
+        } else if (j > 0) {
           // Common case: p = exp2(c s - m) against the running max m.  A row
           // sum <= 2^8 bounds every p of the row by 2^8, i.e. its max grew by
           // at most 8 and the exact path below would keep m: this P is its
@@ -1021,6 +1057,24 @@ __global__ void __launch_bounds__(FwdSpCfg<D>::THREADS, 1)
         else if (ni > 0)
           mbar_wait(bar_item, (ni - 1) & 1, p.err, 15);
         tc_fence_after();
+        if (FP8V && grew) {
+          // this tile's previous PV has completed (the wait above): O_t *= alpha
+          const uint64_t a2 = f2pack(alpha8, alpha8);
+#pragma unroll
+          for (int c = 0; c < D / 16; ++c) {
+            uint32_t o[16];
+            tmem_ld16(tO + c * 16, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+              float lo, hi;
+              f2unpack(fmul2(f2pack(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2), lo, hi);
+              o[e] = __float_as_uint(lo);
+              o[e + 1] = __float_as_uint(hi);
+            }
+            tmem_st16(tO + c * 16, o);
+          }
+        }
         if (!done) {
           // First tile, or a row of this warp may have grown by more than 2^8:
           // tile max, O_t and l rescaled if the max grew by more than 2^8, p.
@@ -1037,7 +1091,7 @@ __global__ void __launch_bounds__(FwdSpCfg<D>::THREADS, 1)
           if (j == 0) {
             m = m_tile;
           } else {
-            const bool need = m_tile > m + kRescaleLog2;
+            const bool need = m_tile > m + kMaxGrowth<FP8V, LAZY8>;
             const float m_new = need ? m_tile : m;
             const float alpha = ex2_approx(m - m_new);
             m = m_new;
@@ -1153,7 +1207,7 @@ __global__ void __launch_bounds__(128) fwd_merge_kernel(const MergeParams mp) {
   if (lane == 0) mp.lse[static_cast<size_t>(bh) * mp.Nq + q] = wsum > 0.f ? mx + logf(wsum) : -CUDART_INF_F;
 }
 
-template <int D, bool BF16, bool FP8V>
+template <int D, bool BF16, bool FP8V, bool LAZY8 = false>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   using C = FwdCfg<D>;
   CUtensorMap tq, tk, tv;
@@ -1186,7 +1240,7 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
   if constexpr (kSepP<D>) {
     using CS = FwdSpCfg<D>;
-    auto kern = fwd_sp_kernel<D, BF16, FP8V>;
+    auto kern = fwd_sp_kernel<D, BF16, FP8V, LAZY8>;
     // setmaxnreg.inc waits until the block's launch registers cover the
     // split: never launch a build whose register count would not.
     static const int num_regs = [&] {
@@ -1217,7 +1271,7 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     }
     kern<<<static_cast<unsigned>(grid), CS::THREADS, CS::SMEM, stream>>>(tq, tk, tv, p);
   } else {
-    auto kern = fwd_kernel<D, BF16, FP8V>;
+    auto kern = fwd_kernel<D, BF16, FP8V, LAZY8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     kern<<<static_cast<unsigned>(blocks), C::THREADS, C::SMEM, stream>>>(tq, tk, tv, p);
@@ -1245,6 +1299,19 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
+  if (a.fp8v && a.fp8_lazy) {
+    if (a.n_splits > 1) return cudaErrorInvalidValue;
+    switch (a.d) {
+      case 64:
+        return a.bf16 ? launch_fwd_t<64, true, true, true>(a, stream) : launch_fwd_t<64, false, true, true>(a, stream);
+      case 80:
+        return a.bf16 ? launch_fwd_t<80, true, true, true>(a, stream) : launch_fwd_t<80, false, true, true>(a, stream);
+      case 128:
+        return a.bf16 ? launch_fwd_t<128, true, true, true>(a, stream)
+                      : launch_fwd_t<128, false, true, true>(a, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   if (a.fp8v) {
     if (a.n_splits > 1) return cudaErrorInvalidValue;
     switch (a.d) {

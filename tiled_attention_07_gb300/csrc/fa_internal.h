@@ -31,6 +31,8 @@ struct FwdArgs {
   // the PV product.
   bool fp8v = false;
   int64_t vt_ld = 0;
+  // e5m2 P under the lazy running-max rule instead of the page's steps
+  bool fp8_lazy = false;
 };
 
 struct BwdArgs {

@@ -46,6 +46,9 @@ FA_BWD_PREPROCESS = 1
 FA_BWD_DKDV = 2
 FA_BWD_DQ = 3
 
+FA_FP8V_PAGE_STEPS = 0
+FA_FP8V_LAZY_MAX = 1
+
 FA_BWD_PATH_AUTO = 0
 FA_BWD_PATH_TWO_PASS = 1
 FA_BWD_PATH_FUSED = 2
@@ -57,6 +60,7 @@ EXPORTED_SYMBOLS = (
     "fa_fwd_split_count",
     "fa_fwd_split",
     "fa_fwd_fp8v",
+    "fa_fwd_fp8v_ex",
     "fa_bwd_workspace_bytes",
     "fa_bwd",
     "fa_bwd_strided",
@@ -116,6 +120,8 @@ def lib() -> ctypes.CDLL:
         L.fa_fwd_split.restype = i
         L.fa_fwd_fp8v.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.c_int64, f, i, i, vp]
         L.fa_fwd_fp8v.restype = i
+        L.fa_fwd_fp8v_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.c_int64, f, i, i, i, vp]
+        L.fa_fwd_fp8v_ex.restype = i
         L.fa_bwd_workspace_bytes.argtypes = [i, i, i, i, i]
         L.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
         L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, ctypes.c_size_t, vp]
@@ -264,11 +270,12 @@ def fa_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, l
 
 
 def fa_fwd_fp8v(q: torch.Tensor, k: torch.Tensor, vt: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
-                sm_scale: float, causal: bool, stream=None) -> None:
+                sm_scale: float, causal: bool, stream=None, mode: int = FA_FP8V_PAGE_STEPS) -> None:
     """The forward with V in float8 e5m2, transposed: ``vt`` is [B, H, d, ld]
     (torch.float8_e5m2 or its raw uint8 codes) with unit stride along keys,
     ld = vt.stride(2) >= Nk and a multiple of 16; q, k, o contiguous
-    [B, H, seq, d] fp16/bf16."""
+    [B, H, seq, d] fp16/bf16.  ``mode``: FA_FP8V_PAGE_STEPS (the page's
+    running max, moved at every block) or FA_FP8V_LAZY_MAX (fa_fwd_fp8v_ex)."""
     B, H, Nq, d = _dims(q)
     _, _, Nk, _ = _dims(k)
     dt = _dtype_code(q)
@@ -286,8 +293,8 @@ def fa_fwd_fp8v(q: torch.Tensor, k: torch.Tensor, vt: torch.Tensor, o: torch.Ten
         if not _is_bhsd_contiguous(t):
             raise ValueError("q, k and o must be contiguous [B, H, seq, d]")
     with torch.cuda.device(q.device):
-        rc = lib().fa_fwd_fp8v(_ptr(q), _ptr(k), _ptr(vt), _ptr(o), _ptr(lse), B, H, Nq, Nk, d, int(ld),
-                               float(sm_scale), int(bool(causal)), dt, _stream(stream, q.device))
+        rc = lib().fa_fwd_fp8v_ex(_ptr(q), _ptr(k), _ptr(vt), _ptr(o), _ptr(lse), B, H, Nq, Nk, d, int(ld),
+                                  float(sm_scale), int(bool(causal)), dt, int(mode), _stream(stream, q.device))
     if rc != FA_OK:
         raise FaError(rc, "fa_fwd_fp8v")
 
