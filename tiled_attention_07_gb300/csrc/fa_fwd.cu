@@ -148,6 +148,40 @@ __device__ __forceinline__ void store_o_lse(const FwdParams& p, uint32_t tO, int
   if (valid) p.lse[(static_cast<int64_t>(b) * p.H + h) * p.Nq + qrow] = (m + log2f(l)) * 0.69314718055994531f;
 }
 
+// store_o_lse with every O column read out of TMEM before one wait (the
+// separate-P forward's epilogue, where the softmax warps' score and P
+// registers are free by then).
+template <int D, bool BF16>
+__device__ __forceinline__ void store_o_lse_batched(const FwdParams& p, uint32_t tO, int b, int h, int qrow, float m,
+                                                    float l) {
+  uint32_t o[D / 16][16];
+#pragma unroll
+  for (int c = 0; c < D / 16; ++c) tmem_ld16(tO + c * 16, o[c]);
+  tmem_wait_ld();
+  const float inv_l = 1.f / l;
+  const bool valid = qrow < p.Nq;
+  uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
+                  2 * (static_cast<int64_t>(b) * p.o_sb + static_cast<int64_t>(h) * p.o_sh +
+                       static_cast<int64_t>(qrow) * p.o_ss);
+#pragma unroll
+  for (int c = 0; c < D / 16; ++c) {
+    uint4 w0, w1;
+    w0.x = pack2<BF16>(__uint_as_float(o[c][0]) * inv_l, __uint_as_float(o[c][1]) * inv_l);
+    w0.y = pack2<BF16>(__uint_as_float(o[c][2]) * inv_l, __uint_as_float(o[c][3]) * inv_l);
+    w0.z = pack2<BF16>(__uint_as_float(o[c][4]) * inv_l, __uint_as_float(o[c][5]) * inv_l);
+    w0.w = pack2<BF16>(__uint_as_float(o[c][6]) * inv_l, __uint_as_float(o[c][7]) * inv_l);
+    w1.x = pack2<BF16>(__uint_as_float(o[c][8]) * inv_l, __uint_as_float(o[c][9]) * inv_l);
+    w1.y = pack2<BF16>(__uint_as_float(o[c][10]) * inv_l, __uint_as_float(o[c][11]) * inv_l);
+    w1.z = pack2<BF16>(__uint_as_float(o[c][12]) * inv_l, __uint_as_float(o[c][13]) * inv_l);
+    w1.w = pack2<BF16>(__uint_as_float(o[c][14]) * inv_l, __uint_as_float(o[c][15]) * inv_l);
+    if (valid) {
+      reinterpret_cast<uint4*>(orow + c * 32)[0] = w0;
+      reinterpret_cast<uint4*>(orow + c * 32)[1] = w1;
+    }
+  }
+  if (valid) p.lse[(static_cast<int64_t>(b) * p.H + h) * p.Nq + qrow] = (m + log2f(l)) * 0.69314718055994531f;
+}
+
 // Epilogue of one query row in split mode: the split's own softmax output
 // O_s = O_acc / l and lse_s = ln 2 * (m + log2 l) in float32, or O_s = 0 and
 // lse_s = -inf when the row saw no key of the split (have == false).
@@ -1133,7 +1167,7 @@ __global__ void __launch_bounds__(FwdSpCfg<D>::THREADS, 1)
       if (p.n_splits > 1)
         store_partial<D>(p, tO, it.bh, it.split, qrow, m, l, n > 0);
       else if (n > 0)
-        store_o_lse<D, BF16>(p, tO, it.b, it.h, qrow, m, l);
+        store_o_lse_batched<D, BF16>(p, tO, it.b, it.h, qrow, m, l);
 
       ni += it.n_max > 0 ? 1 : 0;
 #pragma unroll
