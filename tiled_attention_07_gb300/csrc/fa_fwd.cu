@@ -102,6 +102,9 @@ struct FwdParams {
   // other blocks take one item each of the remaining units (see sp_next).
   int grid_p = 0;
   int persist_units = 0;
+  // Separate-P forward on a grid under one wave: one 128-row query tile per
+  // block (tile 1 of every item empty), so that twice as many SMs work.
+  int single_tile = 0;
 };
 
 // Number of key tiles query tile t (rows r0 .. r0+127) needs.
@@ -700,12 +703,14 @@ __device__ __forceinline__ SpItem sp_item(const FwdParams& p, int rank, int bh, 
   const int pair = p.n_pairs - 1 - rank;
   it.b = bh / p.H;
   it.h = bh % p.H;
-  it.q0 = pair * (kNQT * kBM);
+  it.q0 = pair * (p.single_tile ? kBM : kNQT * kBM);
   it.kt0 = split * p.tiles_per_split;
   it.n_max = 0;
 #pragma unroll
   for (int t = 0; t < kNQT; ++t) {
-    it.nkt[t] = max(0, min(key_tiles(it.q0 + t * kBM, p.Nq, p.Nk, p.causal), it.kt0 + p.tiles_per_split) - it.kt0);
+    it.nkt[t] = t > 0 && p.single_tile
+                    ? 0
+                    : max(0, min(key_tiles(it.q0 + t * kBM, p.Nq, p.Nk, p.causal), it.kt0 + p.tiles_per_split) - it.kt0);
     it.n_max = max(it.n_max, it.nkt[t]);
   }
   return it;
@@ -1164,10 +1169,12 @@ __global__ void __launch_bounds__(FwdSpCfg<D>::THREADS, 1)
         ++on;
         tc_fence_after();
       }
-      if (p.n_splits > 1)
-        store_partial<D>(p, tO, it.bh, it.split, qrow, m, l, n > 0);
-      else if (n > 0)
+      if (p.n_splits > 1) {
+        // (with one query tile per block, tile 1's rows belong to the next block)
+        if (t == 0 || !p.single_tile) store_partial<D>(p, tO, it.bh, it.split, qrow, m, l, n > 0);
+      } else if (n > 0) {
         store_o_lse_batched<D, BF16>(p, tO, it.b, it.h, qrow, m, l);
+      }
 
       ni += it.n_max > 0 ? 1 : 0;
 #pragma unroll
@@ -1285,16 +1292,23 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
       return cudaErrorInvalidConfiguration;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CS::SMEM);
     if (e != cudaSuccess) return e;
-    // Persistent blocks for all but about one round of the units (see
-    // sp_next), when every item gives tile 0 keys and tile 1 at least as
-    // many: no split, and no pair whose second tile lies wholly past Nq.
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
     long long grid = blocks;
     const int pair_rows = kNQT * kBM;
-    if (n_splits == 1 && (a.Nq % pair_rows == 0 || a.Nq % pair_rows > kBM)) {
-      int dev = 0, sms = 0;
-      e = cudaGetDevice(&dev);
-      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-      if (e != cudaSuccess) return e;
+    const int n_tiles = (a.Nq + kBM - 1) / kBM;
+    const long long tile_blocks = static_cast<long long>(n_tiles) * a.B * a.H * n_splits;
+    if (blocks < sms && tile_blocks > blocks && tile_blocks <= sms) {
+      // Under one wave: one query tile per block still fits in one wave.
+      p.single_tile = 1;
+      p.n_pairs = n_tiles;
+      grid = tile_blocks;
+    } else if (n_splits == 1 && (a.Nq % pair_rows == 0 || a.Nq % pair_rows > kBM)) {
+      // Persistent blocks for all but about one round of the units (see
+      // sp_next), when every item gives tile 0 keys and tile 1 at least as
+      // many: no split, and no pair whose second tile lies wholly past Nq.
       const long long units = static_cast<long long>((p.n_pairs + 1) / 2) * a.B * a.H;
       const long long rounds = sms > 0 ? units / sms - 1 : 0;
       if (rounds >= 1) {
