@@ -155,6 +155,7 @@ struct BwdCfg {
   static constexpr int DS_TILE = 128 * 128 * 2;
   static constexpr int DQ_TILE = 128 * D * 4;
   static constexpr int KVQ_SMEM = 1024 + 2 * TILE + KVQ_NSTAGE * KV_STAGE + DS_TILE + DQ_TILE + 512;
+  static_assert(D != 64 || KVQ_SMEM <= 227 * 1024, "the fused layout's shared memory");
   // dQ: Q, dO resident; ring of (K_j, V_j)
   static constexpr int Q_NSTAGE = D == 64 ? 5 : (D == 80 ? 3 : 2);
   static constexpr int Q_STAGE = 2 * TILE;
