@@ -140,8 +140,9 @@ FA_API size_t fa_fwd_split_workspace_bytes(int B, int H, int Nq, int d, int n_sp
 /*
  * fa_fwd_split_count -- a split count for this problem on the current device:
  * the most splits for which the split grid still fits in one wave (one CTA
- * per SM) while every split keeps at least 4 of the 128-key tiles, capped at
- * FA_MAX_SPLITS; 1 when the unsplit grid already fills the SMs.  (Each CTA
+ * per 128-row query tile and split, one CTA per SM) while every split keeps
+ * at least 4 of the 128-key tiles, capped at FA_MAX_SPLITS; 1 when the
+ * unsplit grid already fills the SMs.  (Each CTA
  * has a fixed start-up and drain cost of a few key tiles' work, so more
  * splits than that are slower.)  Returns 1 for invalid or empty problems.
  */
@@ -155,7 +156,9 @@ FA_API int fa_fwd_split_count(int B, int H, int Nq, int Nk, int d, int causal);
  * needs no workspace; otherwise workspace (device, 16-byte aligned, owned by
  * the caller, contents on entry ignored) must hold
  * fa_fwd_split_workspace_bytes(B, H, Nq, d, n_splits) bytes, else
- * FA_ERR_WORKSPACE.  Two launches on `stream` (partial forward, merge).
+ * FA_ERR_WORKSPACE.  Two launches on `stream`: the partial forward, and the
+ * merge as its programmatic dependent (its blocks start as the forward's
+ * finish and wait for the forward's results).
  */
 FA_API fa_status fa_fwd_split(const void* q, const void* k, const void* v, void* o, float* lse,
                        int B, int H, int Nq, int Nk, int d, float sm_scale, int causal,

@@ -79,10 +79,14 @@ def test_one_split_equals_fa_fwd_bitwise():
 
 def test_split_count_stays_in_one_wave():
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    # 4 query-tile pairs x 16 heads = 64 CTAs unsplit, 20 key tiles
+    # 8 query tiles x 16 heads = 128 one-tile CTAs unsplit, 20 key tiles
     s = fa.fa_fwd_split_count(1, 16, 1000, 2500, 80, False)
-    assert s == max(1, min(sms // 64, 20 // 4))
-    assert 64 * s <= max(sms, 64)
+    assert s == max(1, min(sms // 128, 20 // 4))
+    assert 128 * s <= max(sms, 128)
+    # 4 heads: 32 one-tile CTAs, a split grid of several per query tile
+    s = fa.fa_fwd_split_count(1, 4, 1000, 2500, 80, False)
+    assert s == max(1, min(sms // 32, 20 // 4))
+    assert 32 * s <= max(sms, 32)
     # few key tiles per query tile: no split
     assert fa.fa_fwd_split_count(4, 12, 512, 512, 64, True) == 1
     # the bench workload fills the GPU unsplit

@@ -388,9 +388,11 @@ int fa_fwd_split_count(int B, int H, int Nq, int Nk, int d, int causal) {
     return 1;
   // Every CTA pays a fixed start-up and drain time of a few key tiles' work,
   // so a split only pays while the split grid still runs in one wave and
-  // every split keeps at least kMinTilesPerSplit key tiles.
+  // every split keeps at least kMinTilesPerSplit key tiles.  Under one wave
+  // the forward runs one 128-row query tile per CTA, so the unsplit grid to
+  // beat is that one.
   constexpr long long kMinTilesPerSplit = 4;
-  const long long ctas = static_cast<long long>((Nq + 255) / 256) * B * H;   // two query tiles per CTA
+  const long long ctas = static_cast<long long>((Nq + 127) / 128) * B * H;   // one query tile per CTA
   const long long n_kt = (Nk + 127) / 128;
   long long s = sms / ctas;
   if (s > n_kt / kMinTilesPerSplit) s = n_kt / kMinTilesPerSplit;

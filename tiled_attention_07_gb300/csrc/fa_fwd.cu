@@ -296,6 +296,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using C = FwdCfg<D>;
+  if (p.n_splits > 1) griddep_launch_dependents();   // the merge may take SMs as blocks of this grid finish
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
@@ -791,6 +792,7 @@ __global__ void __launch_bounds__(FwdSpCfg<D>::THREADS, 1)
     fwd_sp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using C = FwdSpCfg<D>;
+  if (p.n_splits > 1) griddep_launch_dependents();   // the merge may take SMs as blocks of this grid finish
   constexpr int NS = C::NSTAGE;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1206,6 +1208,9 @@ struct MergeParams {
 
 template <int D, bool BF16>
 __global__ void __launch_bounds__(128) fwd_merge_kernel(const MergeParams mp) {
+  // Launched as a programmatic dependent of the partial forward: its blocks
+  // may start before that grid ends, and wait here for its partials.
+  griddep_wait();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const long long r = static_cast<long long>(blockIdx.x) * 4 + warp;
@@ -1340,8 +1345,17 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   mp.o_ss = p.o_ss;
   mp.lse = a.lse;
   const long long rows = static_cast<long long>(mp.BH) * a.Nq;
-  fwd_merge_kernel<D, BF16><<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(mp);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((rows + 3) / 4));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fwd_merge_kernel<D, BF16>, mp);
 }
 
 }  // namespace
