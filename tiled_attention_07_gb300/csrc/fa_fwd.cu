@@ -81,6 +81,16 @@ struct FwdCfg {
   static constexpr int MMA_WARP = kNQT * 4 + 1;   // first of kNQT issuer warps (also allocates TMEM)
 };
 
+// Programmatic dependent launch.  launch_dependents: once every block of
+// this grid has issued it (or exited), the grid launched after it on the
+// stream with the programmatic-serialization attribute may start.  wait:
+// blocks until the grids this one depends on have completed and their memory
+// operations are visible to it.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 struct FwdParams {
   int B, H, Nq, Nk;
   int n_pairs;          // ceil(Nq / 256)

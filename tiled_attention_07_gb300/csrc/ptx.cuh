@@ -75,16 +75,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Programmatic dependent launch.  launch_dependents: once every block of
-// this grid has issued it (or exited), the grid launched after it on the
-// stream with the programmatic-serialization attribute may start.  wait:
-// blocks until the grids this one depends on have completed and their memory
-// operations are visible to it.
-__device__ __forceinline__ void griddep_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 // Wait until the phase with the given parity has completed.  Bounded: gives up
 // after kWaitLimitNs, or at once when another thread has already given up
 // (the error word is non-zero), recording `site` in the error word.  Returns
