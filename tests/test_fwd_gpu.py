@@ -118,6 +118,37 @@ def test_persistent_units(case):
     print(w.name, stats)
 
 
+# d = 64 shapes whose two-tile grid is under one wave while their one-tile
+# grid (query tiles x heads) is between one and two blocks per SM on a 152-SM
+# part: the forward runs its one-tile build, two blocks to an SM.
+TWO_PER_SM = [
+    # dtype, layout, B, H, Nq, Nk, d, causal
+    ("fp16", "bhsd", 1, 100, 256, 256, 64, False),   # 200 one-tile blocks
+    ("bf16", "bhsd", 1, 90, 200, 700, 64, True),     # ragged second tile, causal with Nq < Nk
+    ("bf16", "shd", 1, 60, 300, 300, 64, True),      # [seq, heads, d], three tiles per head
+    ("fp16", "bhsd", 1, 48, 513, 129, 64, True),     # causal with Nq > Nk: late tiles see every key
+]
+
+
+@pytest.mark.parametrize("case", TWO_PER_SM, ids=["-".join(map(str, c)) for c in TWO_PER_SM])
+def test_one_tile_build_two_per_sm(case):
+    dt, layout, B, H, Nq, Nk, d, causal = case
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    tiles, pairs = (Nq + 127) // 128, (Nq + 255) // 256
+    print("one-tile build taken:", pairs * B * H < sms < tiles * B * H <= 2 * sms)
+    w = W.custom(dt, layout, B, H, Nq, Nk, d, causal, std=0.5 if dt == "fp16" else 1.0, seed=Nq + 3 * H)
+    x = W.make_inputs(w, device="cuda")
+    o, lse = run_fwd(w, x, guard=1024)
+    stats = {}
+    heads = [(b, h) for b in range(B) for h in range(H)]
+    for b, h in heads[:2] + heads[len(heads) // 2:len(heads) // 2 + 1] + heads[-2:]:
+        check_fwd_head(w, x, o, lse, b, h, stats)
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    o2, lse2 = run_fwd(w, x)
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    print(w.name, stats)
+
+
 def test_large_logits_trigger_rescaling():
     # q, k spread widely so that running maxima jump by more than 2^8 between
     # key tiles (checks the lazy O rescaling); v stays N(0, 1) so that |O|

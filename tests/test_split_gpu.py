@@ -61,6 +61,7 @@ def test_named_workloads_all_heads(name, n_splits):
     ("fp16", "bhsd", 1, 2, 129, 77, 64, True, 2),       # one key tile: split 1 empty for everyone
     ("bf16", "shd", 1, 4, 1000, 2500, 80, True, 6),     # [seq, heads, d], causal with Nq < Nk
     ("fp16", "bhsd", 1, 1, 1, 1000, 64, False, 8),      # a single query row
+    ("bf16", "bhsd", 1, 40, 256, 2048, 64, True, 2),    # one-tile blocks two to an SM (160 on 152 SMs)
 ])
 def test_edge_cases(dtype, layout, B, H, Nq, Nk, d, causal, n_splits):
     w = W.custom(dtype, layout, B, H, Nq, Nk, d, causal, seed=Nq + Nk + n_splits)

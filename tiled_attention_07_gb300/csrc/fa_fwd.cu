@@ -773,41 +773,53 @@ __device__ __forceinline__ bool sp_next(const FwdParams& p, int q, SpItem* it) {
   return true;
 }
 
-template <int D>
+// SMALL: the one-query-tile build for grids of one-tile blocks that fit in
+// one wave only at two blocks per SM (d = 64, 16-bit V): one softmax
+// warpgroup, 256 TMEM columns, a 4-slot ring and a 128-register launch, so
+// that two blocks share an SM and one's start-up overlaps the other's work.
+template <int D, bool SMALL = false>
 struct FwdSpCfg {
   using G = TileGeo<D>;
   static constexpr int TILE = G::TILE;
-  static constexpr int NSTAGE = D == 64 ? 8 : 6;   // even: K_j in even slots, V_j in odd
-  static constexpr int SMEM_DATA = kNQT * TILE + NSTAGE * TILE;
+  static constexpr int NT = SMALL ? 1 : kNQT;        // query tiles with softmax warps
+  static constexpr int NSTAGE = SMALL ? 4 : (D == 64 ? 8 : 6);   // even: K_j in even slots, V_j in odd
+  static constexpr int SMEM_DATA = NT * TILE + NSTAGE * TILE;
   static constexpr int NBARS = 2 * kNQT + 2 * NSTAGE + 4 * kNQT + 3;
   static constexpr int SMEM = 1024 + SMEM_DATA + NBARS * 8 + 16;
-  static constexpr int THREADS = 384;
-  static constexpr int PROD_WARP = 8;
-  static constexpr int MMA_WARP = 9;            // issuer A; issuer B is warp 10
-  static constexpr uint32_t kColO = 256;        // O_t at kColO + t * D
-  static constexpr uint32_t kColP = 256 + 2 * D;
-  // Register split: 384 threads launch with 168 registers each (64,512 in
-  // all); the softmax warpgroups take 224, the third warpgroup keeps 56:
-  // 2 * 128 * 224 + 128 * 56 = 64,512.
-  static constexpr uint32_t kRegSoftmax = 224;
-  static constexpr uint32_t kRegOther = 56;
+  static constexpr int THREADS = NT * 128 + 128;
+  static constexpr int BLOCKS_PER_SM = SMALL ? 2 : 1;
+  static constexpr int LAUNCH_REGS = SMALL ? 128 : 168;   // registers a thread launches with
+  static constexpr int PROD_WARP = NT * 4;
+  static constexpr int MMA_WARP = NT * 4 + 1;   // issuer A; issuer B is the warp after it
+  static constexpr uint32_t TMEM_COLS = SMALL ? 256 : 512;
+  static constexpr uint32_t kColO = NT * 128;   // O_t at kColO + t * D (S_t at t * 128)
+  static constexpr uint32_t kColP = kColO + NT * D;
+  // Register split: the softmax warpgroups grow, the last warpgroup
+  // (producer, issuers) shrinks, within the block's launch registers:
+  // 384 x 168 = 64,512 >= 2 * 128 * 224 + 128 * 56; SMALL: 256 x 128 =
+  // 32,768 >= 128 * 208 + 128 * 48.
+  static constexpr uint32_t kRegSoftmax = SMALL ? 208 : 224;
+  static constexpr uint32_t kRegOther = SMALL ? 48 : 56;
+  static_assert(!SMALL || D == 64, "the one-tile build fits d = 64");
   static_assert(NSTAGE % 2 == 0, "K and V alternate between even and odd slots");
-  static_assert(kColP + 64 <= 512, "TMEM budget");
-  static_assert(2 * 128 * kRegSoftmax + 128 * kRegOther <= THREADS * 168, "register split exceeds the launch");
-  static_assert(SMEM <= 227 * 1024, "shared memory budget");
+  static_assert(kColP + 64 <= TMEM_COLS, "TMEM budget");
+  static_assert(NT * 128 * kRegSoftmax + 128 * kRegOther <= THREADS * LAUNCH_REGS,
+                "register split exceeds the launch");
+  static_assert(SMEM * BLOCKS_PER_SM <= 227 * 1024, "shared memory budget");
 };
 
-template <int D, bool BF16, bool FP8V, bool LAZY8 = false>
-__global__ void __launch_bounds__(FwdSpCfg<D>::THREADS, 1)
+template <int D, bool BF16, bool FP8V, bool LAZY8 = false, bool SMALL = false>
+__global__ void __launch_bounds__(FwdSpCfg<D, SMALL>::THREADS, FwdSpCfg<D, SMALL>::BLOCKS_PER_SM)
     fwd_sp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-  using C = FwdSpCfg<D>;
+  using C = FwdSpCfg<D, SMALL>;
+  static_assert(!SMALL || !FP8V, "the one-tile build takes 16-bit V");
   if (p.n_splits > 1) griddep_launch_dependents();   // the merge may take SMs as blocks of this grid finish
   constexpr int NS = C::NSTAGE;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
-  uint8_t* sKV = smem + kNQT * C::TILE;
+  uint8_t* sKV = smem + C::NT * C::TILE;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + NS * C::TILE);
   uint64_t* bar_q = bars;                      // [kNQT] Q_t landed
   uint64_t* bar_qfree = bar_q + kNQT;          // [kNQT] last S_t of an item complete: Q_t may be replaced
@@ -844,7 +856,7 @@ __global__ void __launch_bounds__(FwdSpCfg<D>::THREADS, 1)
     fence_mbar_init();
   }
   if (warp == C::MMA_WARP) {
-    tmem_alloc(tmem_slot, 512);
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -1198,7 +1210,7 @@ __global__ void __launch_bounds__(FwdSpCfg<D>::THREADS, 1)
   __syncthreads();
   if (warp == C::MMA_WARP) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 
@@ -1315,24 +1327,47 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     const int pair_rows = kNQT * kBM;
     const int n_tiles = (a.Nq + kBM - 1) / kBM;
     const long long tile_blocks = static_cast<long long>(n_tiles) * a.B * a.H * n_splits;
-    if (blocks < sms && tile_blocks > blocks && tile_blocks <= sms) {
-      // Under one wave: one query tile per block still fits in one wave.
-      p.single_tile = 1;
-      p.n_pairs = n_tiles;
-      grid = tile_blocks;
-    } else if (n_splits == 1 && (a.Nq % pair_rows == 0 || a.Nq % pair_rows > kBM)) {
-      // Persistent blocks for all but about one round of the units (see
-      // sp_next), when every item gives tile 0 keys and tile 1 at least as
-      // many: no split, and no pair whose second tile lies wholly past Nq.
-      const long long units = static_cast<long long>((p.n_pairs + 1) / 2) * a.B * a.H;
-      const long long rounds = sms > 0 ? units / sms - 1 : 0;
-      if (rounds >= 1) {
-        p.grid_p = sms;
-        p.persist_units = static_cast<int>(rounds * sms);
-        grid = sms + 2 * (units - p.persist_units);
+    bool small = false;
+    if constexpr (D == 64 && !FP8V) {
+      // Under one wave of two-tile blocks, with one-tile blocks that fill
+      // the SMs but fit two to an SM: the one-tile build, if this build's
+      // launch registers cover its register split.
+      using CM = FwdSpCfg<D, true>;
+      auto km = fwd_sp_kernel<D, BF16, false, false, true>;
+      static const int m_regs = [&] {
+        cudaFuncAttributes fattr{};
+        return cudaFuncGetAttributes(&fattr, km) == cudaSuccess ? fattr.numRegs : 0;
+      }();
+      if (blocks < sms && tile_blocks > sms && tile_blocks <= 2LL * sms &&
+          m_regs * CM::THREADS >= 128 * static_cast<int>(CM::kRegSoftmax) + 128 * static_cast<int>(CM::kRegOther)) {
+        e = cudaFuncSetAttribute(km, cudaFuncAttributeMaxDynamicSharedMemorySize, CM::SMEM);
+        if (e != cudaSuccess) return e;
+        p.single_tile = 1;
+        p.n_pairs = n_tiles;
+        km<<<static_cast<unsigned>(tile_blocks), CM::THREADS, CM::SMEM, stream>>>(tq, tk, tv, p);
+        small = true;
       }
     }
-    kern<<<static_cast<unsigned>(grid), CS::THREADS, CS::SMEM, stream>>>(tq, tk, tv, p);
+    if (!small) {
+      if (blocks < sms && tile_blocks > blocks && tile_blocks <= sms) {
+        // Under one wave: one query tile per block still fits in one wave.
+        p.single_tile = 1;
+        p.n_pairs = n_tiles;
+        grid = tile_blocks;
+      } else if (n_splits == 1 && (a.Nq % pair_rows == 0 || a.Nq % pair_rows > kBM)) {
+        // Persistent blocks for all but about one round of the units (see
+        // sp_next), when every item gives tile 0 keys and tile 1 at least as
+        // many: no split, and no pair whose second tile lies wholly past Nq.
+        const long long units = static_cast<long long>((p.n_pairs + 1) / 2) * a.B * a.H;
+        const long long rounds = sms > 0 ? units / sms - 1 : 0;
+        if (rounds >= 1) {
+          p.grid_p = sms;
+          p.persist_units = static_cast<int>(rounds * sms);
+          grid = sms + 2 * (units - p.persist_units);
+        }
+      }
+      kern<<<static_cast<unsigned>(grid), CS::THREADS, CS::SMEM, stream>>>(tq, tk, tv, p);
+    }
   } else {
     auto kern = fwd_kernel<D, BF16, FP8V, LAZY8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
