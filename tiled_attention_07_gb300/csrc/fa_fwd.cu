@@ -773,10 +773,10 @@ __device__ __forceinline__ bool sp_next(const FwdParams& p, int q, SpItem* it) {
   return true;
 }
 
-// SMALL: the one-query-tile build for grids of one-tile blocks that fit in
-// one wave only at two blocks per SM (d = 64, 16-bit V): one softmax
+// SMALL: the one-query-tile build (d = 64, 16-bit V): one softmax
 // warpgroup, 256 TMEM columns, a 4-slot ring and a 128-register launch, so
-// that two blocks share an SM and one's start-up overlaps the other's work.
+// that two blocks share an SM; each tile's K/V stream is its own, and the two
+// blocks of an SM run out of step with each other.
 template <int D, bool SMALL = false>
 struct FwdSpCfg {
   using G = TileGeo<D>;
@@ -1329,22 +1329,38 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     const long long tile_blocks = static_cast<long long>(n_tiles) * a.B * a.H * n_splits;
     bool small = false;
     if constexpr (D == 64 && !FP8V) {
-      // Under one wave of two-tile blocks, with one-tile blocks that fill
-      // the SMs but fit two to an SM: the one-tile build, if this build's
-      // launch registers cover its register split.
+      // The one-tile build, two blocks per SM, whenever one-tile blocks
+      // outnumber the SMs: unsplit, or split with the two-tile grid under one
+      // wave and the one-tile grid within two blocks per SM.  Only if this
+      // build's launch registers cover its register split.
       using CM = FwdSpCfg<D, true>;
       auto km = fwd_sp_kernel<D, BF16, false, false, true>;
       static const int m_regs = [&] {
         cudaFuncAttributes fattr{};
         return cudaFuncGetAttributes(&fattr, km) == cudaSuccess ? fattr.numRegs : 0;
       }();
-      if (blocks < sms && tile_blocks > sms && tile_blocks <= 2LL * sms &&
+      const long long slots = 2LL * sms;   // resident one-tile blocks
+      if (tile_blocks > sms && (n_splits == 1 || (blocks < sms && tile_blocks <= slots)) &&
           m_regs * CM::THREADS >= 128 * static_cast<int>(CM::kRegSoftmax) + 128 * static_cast<int>(CM::kRegOther)) {
         e = cudaFuncSetAttribute(km, cudaFuncAttributeMaxDynamicSharedMemorySize, CM::SMEM);
         if (e != cudaSuccess) return e;
         p.single_tile = 1;
         p.n_pairs = n_tiles;
-        km<<<static_cast<unsigned>(tile_blocks), CM::THREADS, CM::SMEM, stream>>>(tq, tk, tv, p);
+        long long grid_m = tile_blocks;
+        if (n_splits == 1) {
+          // Walking blocks, two per SM, for all but about one round of the
+          // units (a unit: the query tiles of ranks r and n_tiles - 1 - r of
+          // one head; see sp_next).  With one tile per item every non-empty
+          // item has tile 0 keys, so no shape condition is needed.
+          const long long units = static_cast<long long>((n_tiles + 1) / 2) * a.B * a.H;
+          const long long rounds = units / slots - 1;
+          if (rounds >= 1) {
+            p.grid_p = static_cast<int>(slots);
+            p.persist_units = static_cast<int>(rounds * slots);
+            grid_m = slots + 2 * (units - p.persist_units);
+          }
+        }
+        km<<<static_cast<unsigned>(grid_m), CM::THREADS, CM::SMEM, stream>>>(tq, tk, tv, p);
         small = true;
       }
     }
