@@ -773,7 +773,7 @@ __device__ __forceinline__ bool sp_next(const FwdParams& p, int q, SpItem* it) {
   return true;
 }
 
-// SMALL: the one-query-tile build (d = 64, 16-bit V): one softmax
+// SMALL: the one-query-tile build (d = 64): one softmax
 // warpgroup, 256 TMEM columns, a 4-slot ring and a 128-register launch, so
 // that two blocks share an SM; each tile's K/V stream is its own, and the two
 // blocks of an SM run out of step with each other.
@@ -813,7 +813,6 @@ __global__ void __launch_bounds__(FwdSpCfg<D, SMALL>::THREADS, FwdSpCfg<D, SMALL
     fwd_sp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using C = FwdSpCfg<D, SMALL>;
-  static_assert(!SMALL || !FP8V, "the one-tile build takes 16-bit V");
   if (p.n_splits > 1) griddep_launch_dependents();   // the merge may take SMs as blocks of this grid finish
   constexpr int NS = C::NSTAGE;
   extern __shared__ uint8_t smem_raw[];
@@ -1328,13 +1327,13 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     const int n_tiles = (a.Nq + kBM - 1) / kBM;
     const long long tile_blocks = static_cast<long long>(n_tiles) * a.B * a.H * n_splits;
     bool small = false;
-    if constexpr (D == 64 && !FP8V) {
+    if constexpr (D == 64) {
       // The one-tile build, two blocks per SM, whenever one-tile blocks
       // outnumber the SMs: unsplit, or split with the two-tile grid under one
       // wave and the one-tile grid within two blocks per SM.  Only if this
       // build's launch registers cover its register split.
       using CM = FwdSpCfg<D, true>;
-      auto km = fwd_sp_kernel<D, BF16, false, false, true>;
+      auto km = fwd_sp_kernel<D, BF16, FP8V, LAZY8, true>;
       static const int m_regs = [&] {
         cudaFuncAttributes fattr{};
         return cudaFuncGetAttributes(&fattr, km) == cudaSuccess ? fattr.numRegs : 0;
