@@ -93,13 +93,23 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreParams p) {
   const bool valid = active && q < p.Nq;
   float acc = 0.f;
   if (valid) {
+    // 16-byte vectors of the row, at most two per lane (d <= 128), all
+    // loaded before the first product so that a row costs one round trip
+    const int nv = p.d / 8;
     const uint4* po = reinterpret_cast<const uint4*>(row_ptr(p.o, p.o_sb, p.o_sh, p.o_ss, b, h, q));
     const uint4* pd = reinterpret_cast<const uint4*>(row_ptr(p.dout, p.d_sb, p.d_sh, p.d_ss, b, h, q));
-    for (int c = sub; c < p.d / 8; c += 8) {
-      const uint4 a = __ldg(po + c);
-      const uint4 g = __ldg(pd + c);
-      const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
-      const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+    uint4 a[2] = {}, g[2] = {};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      if (sub + 8 * i < nv) {
+        a[i] = __ldg(po + sub + 8 * i);
+        g[i] = __ldg(pd + sub + 8 * i);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const uint32_t aw[4] = {a[i].x, a[i].y, a[i].z, a[i].w};
+      const uint32_t gw[4] = {g[i].x, g[i].y, g[i].z, g[i].w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float2 fa = unpack2<BF16>(aw[e]);
