@@ -11,8 +11,9 @@
 //
 // Two kernels.  fwd_sp_kernel (d <= 96, further below) gives P TMEM columns
 // of its own, splits the issuers by MMA kind (one warp every S, one every PV),
-// lets blocks walk several work units, and has an e5m2-V variant; fwd_kernel
-// (d = 128, next) is described here.
+// lets blocks walk several work units, and has an e5m2-V variant; at d = 64
+// it also has a one-query-tile build that runs two blocks per SM.
+// fwd_kernel (d = 128, next) is described here.
 //
 // GB300 design (one CTA = two 128-row query tiles of one (b, h)):
 //   warps 0-3  softmax / correction / epilogue of query tile 0 (one row each)
